@@ -1,0 +1,255 @@
+"""Python binding of libmla.so: absorbed MLA decode for B300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libmla.so.  PyTorch is used for device memory and streams; the
+functions take torch tensors, pass their device pointers and the current
+CUDA stream to the C ABI (include/mla.h) and raise RuntimeError when a call
+returns a non-OK status.  There is no fallback: importing the package fails
+if libmla.so has not been built (python head_latent_attention_27_b300/build.py).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python head_latent_attention_27_b300/build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE = range(6)
+MLA_BF16, MLA_FP32 = 0, 1
+MLA_APPEND_RMSNORM = 1
+MLA_APPEND_ROPE = 2
+PAGE_SIZE = 64
+
+
+class mla_cache_t(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p),
+        ("page_table", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("num_seqs", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("d_c", ctypes.c_int32),
+        ("d_r", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32),
+    ]
+
+
+_vp, _i32, _u32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t
+_pc = ctypes.POINTER(mla_cache_t)
+
+_SIGS = {
+    "mla_cache_append": (_i32, [_pc, _vp, _vp, _i32, _vp, _f32, _f32, _vp, _vp, _i32, _u32, _vp]),
+    "mla_decode": (_i32, [_pc, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "mla_decode_split_combine": (_i32, [_pc, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "mla_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "mla_decode_plan": (_i32, [_pc, _vp, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "mla_decode_attend": (_i32, [_pc, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "mla_decode_combine": (_i32, [_pc, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "mla_decode_read_status": (_i32, [_vp, _sz, _vp, ctypes.POINTER(_i32)]),
+    "mla_selftest_bounded_wait": (_i32, [_vp, _sz, _u32, _vp]),
+    "mla_status_string": (ctypes.c_char_p, [_i32]),
+    "mla_version": (_i32, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+def mla_status_string(code: int) -> str:
+    return _lib.mla_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != MLA_OK:
+        raise RuntimeError(f"{what}: {mla_status_string(code)}")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return MLA_BF16
+    if t.dtype == torch.float32:
+        return MLA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need(t, name, dtype=None, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+@dataclass
+class Cache:
+    """A paged latent cache: data [num_pages, 64, d_c + d_r] and page_table [B, max_pages]."""
+    data: "object"
+    page_table: "object"
+    d_c: int
+    d_r: int
+
+    def __post_init__(self):
+        torch = _torch()
+        _need(self.data, "cache.data", ndim=3)
+        _need(self.page_table, "cache.page_table", torch.int32, 2)
+        if self.data.shape[1] != PAGE_SIZE or self.data.shape[2] != self.d_c + self.d_r:
+            raise ValueError("cache.data must be [num_pages, 64, d_c + d_r]")
+
+    def c(self) -> mla_cache_t:
+        return mla_cache_t(self.data.data_ptr(), self.page_table.data_ptr(), _dtype_code(self.data),
+                           self.page_table.shape[0], self.data.shape[0], PAGE_SIZE, self.d_c, self.d_r,
+                           self.page_table.shape[1])
+
+
+def mla_cache_append(cache: Cache, ckv_raw, kr_raw, seq_ids, positions, gamma=None, eps: float = 1e-6,
+                     rope_base: float = 10000.0, flags: int = MLA_APPEND_RMSNORM | MLA_APPEND_ROPE,
+                     stream=None) -> None:
+    """Write T tokens: ckv_raw [T, d_c], kr_raw [T, d_r], seq_ids/positions int32 [T]."""
+    torch = _torch()
+    _need(ckv_raw, "ckv_raw", ndim=2)
+    _need(kr_raw, "kr_raw", ckv_raw.dtype, 2)
+    _need(seq_ids, "seq_ids", torch.int32, 1)
+    _need(positions, "positions", torch.int32, 1)
+    T = ckv_raw.shape[0]
+    if kr_raw.shape[0] != T or seq_ids.shape[0] != T or positions.shape[0] != T:
+        raise ValueError("row counts differ")
+    if ckv_raw.shape[1] != cache.d_c or kr_raw.shape[1] != cache.d_r:
+        raise ValueError("row widths do not match the cache")
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, 1)
+    cc = cache.c()
+    _check(_lib.mla_cache_append(ctypes.byref(cc), _ptr(ckv_raw), _ptr(kr_raw), _dtype_code(ckv_raw), _ptr(gamma),
+                                 float(eps), float(rope_base), _ptr(seq_ids), _ptr(positions), T, int(flags),
+                                 _stream(stream)), "mla_cache_append")
+
+
+def mla_decode_workspace_size(B: int, Q: int, H: int, d_c: int = 512, n_split: int = 0, num_sms: int = 0) -> int:
+    n = _lib.mla_decode_workspace_size(B, Q, H, d_c, n_split, num_sms)
+    if n == 0:
+        raise RuntimeError("mla_decode_workspace_size: invalid arguments")
+    return int(n)
+
+
+def alloc_workspace(B: int, Q: int, H: int, d_c: int = 512, n_split: int = 0, device=None):
+    """A uint8 CUDA tensor large enough for a decode of this shape (256-byte aligned)."""
+    torch = _torch()
+    n = mla_decode_workspace_size(B, Q, H, d_c, n_split)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _decode_args(cache: Cache, seq_lens, q_nope, q_rope, out, lse):
+    torch = _torch()
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(q_nope, "q_nope", cache.data.dtype, 4)
+    _need(q_rope, "q_rope", cache.data.dtype, 4)
+    _need(out, "out", cache.data.dtype, 4)
+    B, Q, H, dc = q_nope.shape
+    if dc != cache.d_c or tuple(q_rope.shape) != (B, Q, H, cache.d_r) or tuple(out.shape) != (B, Q, H, cache.d_c):
+        raise ValueError("q_nope/q_rope/out shapes do not match")
+    if seq_lens.shape[0] != B:
+        raise ValueError("seq_lens must have B entries")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+        if tuple(lse.shape) != (B, Q, H):
+            raise ValueError("lse must be [B, Q, H]")
+    return B, Q, H
+
+
+def mla_decode(cache: Cache, seq_lens, q_nope, q_rope, out, lse=None, workspace=None,
+               softmax_scale: float | None = None, d_h: int = 128, stream=None) -> None:
+    """out[b,j,h] = softmax(scale (q_nope.c + q_rope.k_R)) . c over the visible history."""
+    B, Q, H = _decode_args(cache, seq_lens, q_nope, q_rope, out, lse)
+    scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(d_h + cache.d_r)
+    if workspace is None:
+        workspace = alloc_workspace(B, Q, H, cache.d_c, 0, out.device)
+    cc = cache.c()
+    _check(_lib.mla_decode(ctypes.byref(cc), _ptr(seq_lens), B, _ptr(q_nope), _ptr(q_rope), Q, H, float(scale),
+                           _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)), "mla_decode")
+
+
+def mla_decode_split_combine(cache: Cache, seq_lens, q_nope, q_rope, out, n_split: int, lse=None, workspace=None,
+                             softmax_scale: float | None = None, d_h: int = 128, stream=None) -> None:
+    """mla_decode with every sequence cut into n_split chunks, merged by log-sum-exp."""
+    B, Q, H = _decode_args(cache, seq_lens, q_nope, q_rope, out, lse)
+    scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(d_h + cache.d_r)
+    if workspace is None:
+        workspace = alloc_workspace(B, Q, H, cache.d_c, n_split, out.device)
+    cc = cache.c()
+    _check(_lib.mla_decode_split_combine(ctypes.byref(cc), _ptr(seq_lens), B, _ptr(q_nope), _ptr(q_rope), Q, H,
+                                         float(scale), int(n_split), _ptr(out), _ptr(lse), _ptr(workspace),
+                                         workspace.numel(), _stream(stream)), "mla_decode_split_combine")
+
+
+def mla_decode_plan(cache: Cache, seq_lens, Q: int, H: int, workspace, n_split: int = 0, stream=None) -> None:
+    torch = _torch()
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    cc = cache.c()
+    _check(_lib.mla_decode_plan(ctypes.byref(cc), _ptr(seq_lens), seq_lens.shape[0], Q, H, int(n_split),
+                                _ptr(workspace), workspace.numel(), _stream(stream)), "mla_decode_plan")
+
+
+def mla_decode_attend(cache: Cache, seq_lens, q_nope, q_rope, out, workspace, lse=None, n_split: int = 0,
+                      softmax_scale: float | None = None, d_h: int = 128, stream=None) -> None:
+    B, Q, H = _decode_args(cache, seq_lens, q_nope, q_rope, out, lse)
+    scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(d_h + cache.d_r)
+    cc = cache.c()
+    _check(_lib.mla_decode_attend(ctypes.byref(cc), _ptr(seq_lens), B, _ptr(q_nope), _ptr(q_rope), Q, H,
+                                  float(scale), int(n_split), _ptr(out), _ptr(lse), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "mla_decode_attend")
+
+
+def mla_decode_combine(cache: Cache, out, workspace, lse=None, n_split: int = 0, stream=None) -> None:
+    B, Q, H, _ = out.shape
+    cc = cache.c()
+    _check(_lib.mla_decode_combine(ctypes.byref(cc), B, Q, H, int(n_split), _ptr(out), _ptr(lse), _ptr(workspace),
+                                   workspace.numel(), _stream(stream)), "mla_decode_combine")
+
+
+def mla_decode_read_status(workspace, stream=None) -> int:
+    """Synchronise the stream; return and clear the status the kernels recorded."""
+    code = ctypes.c_int32(0)
+    _lib.mla_decode_read_status(_ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(code))
+    return int(code.value)
+
+
+def mla_selftest_bounded_wait(workspace, timeout_us: int = 20000, stream=None) -> None:
+    _check(_lib.mla_selftest_bounded_wait(_ptr(workspace), workspace.numel(), int(timeout_us), _stream(stream)),
+           "mla_selftest_bounded_wait")
+
+
+def mla_version() -> int:
+    return int(_lib.mla_version())

@@ -1,0 +1,367 @@
+// C ABI of libmla.so (declared in include/mla.h): argument checks, the
+// per-device kernel configuration, TMA descriptor encoding and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "append.cuh"
+#include "decode_f32.cuh"
+#include "decode_plan.cuh"
+#include "decode_tc.cuh"
+#include "mla.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int32_t sms = 0;
+    int32_t tc_clusters = 0;  // co-resident 2-CTA clusters of the tensor-core kernel
+    cudaError_t err = cudaSuccess;
+};
+
+std::once_flag g_once[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+
+const DeviceInfo* device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::call_once(g_once[dev], [dev]() {
+        DeviceInfo& d = g_info[dev];
+        int sms = 0;
+        d.err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err != cudaSuccess) return;
+        d.sms = sms;
+        int32_t cl = 0;
+        d.err = decode_tc_max_clusters(&cl);
+        if (d.err != cudaSuccess) return;
+        d.tc_clusters = cl < sms / 2 ? cl : sms / 2;
+    });
+    return &g_info[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map: rows x cols (row stride `stride_elems`), box
+// box_cols x box_rows.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t stride_elems,
+               uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {stride_elems * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status_t check_cache(const mla_cache_t* c) {
+    if (!c || !c->data || !c->page_table) return MLA_ERR_INVALID_ARG;
+    if (c->dtype != MLA_BF16 && c->dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+    if (c->num_seqs < 1 || c->num_pages < 1 || c->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
+    if (c->num_pages > (1 << 24) || (int64_t)c->max_pages_per_seq * kTileTokens > (1 << 30))
+        return MLA_ERR_INVALID_ARG;
+    if (c->page_size != kTileTokens) return MLA_ERR_UNSUPPORTED;
+    if (c->d_c < 1 || c->d_r < 0 || (c->d_r & 1)) return MLA_ERR_INVALID_ARG;
+    if (c->dtype == MLA_BF16) {
+        if (c->d_c != 512 || c->d_r != 64) return MLA_ERR_UNSUPPORTED;
+        if (!aligned16(c->data)) return MLA_ERR_INVALID_ARG;
+    } else {
+        if (c->d_c > 512 || (c->d_c & 3) || c->d_r > 64) return MLA_ERR_UNSUPPORTED;
+        if ((reinterpret_cast<uintptr_t>(c->data) & 3u) != 0) return MLA_ERR_INVALID_ARG;
+    }
+    return MLA_OK;
+}
+
+int32_t num_workers(const DeviceInfo* d, int32_t dtype) {
+    return dtype == MLA_BF16 ? d->tc_clusters : d->sms;
+}
+
+struct DecodeShape {
+    int32_t B, Q, H, n_split;
+};
+
+mla_status_t check_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeShape s, const void* q_nope,
+                          const void* q_rope, const void* out) {
+    mla_status_t st = check_cache(c);
+    if (st != MLA_OK) return st;
+    if (s.B < 0 || s.B > c->num_seqs || s.Q < 1 || s.H < 1) return MLA_ERR_INVALID_ARG;
+    if ((int64_t)s.Q * s.H > 4096) return MLA_ERR_UNSUPPORTED;
+    if (s.n_split < 0 || s.n_split > kMaxSplit) return MLA_ERR_INVALID_ARG;
+    if (s.B > 0 && (!seq_lens || !q_nope || !out || (c->d_r > 0 && !q_rope))) return MLA_ERR_INVALID_ARG;
+    if ((int64_t)s.B * s.Q * s.H > (int64_t)1 << 30) return MLA_ERR_UNSUPPORTED;
+    if (c->dtype == MLA_BF16 && s.B > 0 && (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(out)))
+        return MLA_ERR_INVALID_ARG;
+    return MLA_OK;
+}
+
+mla_status_t check_workspace(void* ws, size_t bytes, const WsLayout& L) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MLA_ERR_WORKSPACE;
+    if (bytes < L.total) return MLA_ERR_WORKSPACE;
+    return MLA_OK;
+}
+
+mla_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+mla_status_t do_plan(const mla_cache_t* c, const int32_t* seq_lens, DecodeShape s, void* ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+    const DeviceInfo* d = device_info();
+    if (!d || d->err != cudaSuccess || d->sms <= 0) return MLA_ERR_CUDA;
+    const int32_t P = num_workers(d, c->dtype);
+    if (P <= 0) return MLA_ERR_CUDA;
+    const WsLayout L = ws_layout(s.B, s.Q, s.H, c->d_c, s.n_split, P);
+    mla_status_t st = check_workspace(ws, ws_bytes, L);
+    if (st != MLA_OK) return st;
+    return cuda_status(launch_plan(seq_lens, s.B, s.Q, s.H, s.n_split, P, c->max_pages_per_seq * kTileTokens, ws,
+                                   L, stream));
+}
+
+mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShape s, const void* q_nope,
+                       const void* q_rope, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+    const DeviceInfo* d = device_info();
+    if (!d || d->err != cudaSuccess || d->sms <= 0) return MLA_ERR_CUDA;
+    const int32_t P = num_workers(d, c->dtype);
+    const WsLayout L = ws_layout(s.B, s.Q, s.H, c->d_c, s.n_split, P);
+    mla_status_t st = check_workspace(ws, ws_bytes, L);
+    if (st != MLA_OK) return st;
+    if (s.B == 0) return MLA_OK;
+    if (c->dtype == MLA_FP32) {
+        F32Args a;
+        a.cache = static_cast<const float*>(c->data);
+        a.page_table = c->page_table;
+        a.seq_lens = seq_lens;
+        a.q_nope = static_cast<const float*>(q_nope);
+        a.q_rope = static_cast<const float*>(q_rope);
+        a.out = static_cast<float*>(out);
+        a.lse = lse;
+        a.num_pages = c->num_pages;
+        a.max_pages_per_seq = c->max_pages_per_seq;
+        a.d_c = c->d_c;
+        a.d_r = c->d_r;
+        a.Q = s.Q;
+        a.H = s.H;
+        a.scale = scale;
+        return cuda_status(launch_decode_f32(a, P, ws, L, stream));
+    }
+    TcMaps maps;
+    const uint64_t cache_rows = (uint64_t)c->num_pages * kTileTokens;
+    const uint64_t qrows = (uint64_t)s.B * s.Q * s.H;
+    if (!encode_2d(&maps.kv_nope, c->data, cache_rows, 576, 576, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&maps.kv_rope, c->data, cache_rows, 576, 576, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_2d(&maps.q_nope, q_nope, qrows, 512, 512, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&maps.q_rope, q_rope, qrows, 64, 64, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+        return MLA_ERR_CUDA;
+    TcArgs a;
+    a.page_table = c->page_table;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.lse = lse;
+    a.num_pages = c->num_pages;
+    a.max_pages_per_seq = c->max_pages_per_seq;
+    a.Q = s.Q;
+    a.H = s.H;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.evict_first = units_per_seq(s.Q, s.H) == 1 ? 1 : 0;
+    return cuda_status(launch_decode_tc(maps, a, P, ws, L, stream));
+}
+
+mla_status_t do_combine(const mla_cache_t* c, DecodeShape s, void* out, float* lse, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+    const DeviceInfo* d = device_info();
+    if (!d || d->err != cudaSuccess || d->sms <= 0) return MLA_ERR_CUDA;
+    const int32_t P = num_workers(d, c->dtype);
+    const WsLayout L = ws_layout(s.B, s.Q, s.H, c->d_c, s.n_split, P);
+    mla_status_t st = check_workspace(ws, ws_bytes, L);
+    if (st != MLA_OK) return st;
+    if (s.B == 0) return MLA_OK;
+    return cuda_status(launch_combine(s.B, s.Q, s.H, c->d_c, c->dtype, out, lse, ws, L, stream));
+}
+
+mla_status_t run_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeShape s, const void* q_nope,
+                        const void* q_rope, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+    mla_status_t st = check_decode(c, seq_lens, s, q_nope, q_rope, out);
+    if (st != MLA_OK) return st;
+    if (s.B == 0) return MLA_OK;
+    st = do_plan(c, seq_lens, s, ws, ws_bytes, stream);
+    if (st != MLA_OK) return st;
+    st = do_attend(c, seq_lens, s, q_nope, q_rope, scale, out, lse, ws, ws_bytes, stream);
+    if (st != MLA_OK) return st;
+    return do_combine(c, s, out, lse, ws, ws_bytes, stream);
+}
+
+// ------------------------------------------------- bounded-wait self-test --
+
+__global__ void selftest_wait_kernel(int* status, uint32_t timeout_us) {
+    __shared__ __align__(8) uint64_t mbar;
+    const uint32_t bar = smem_addr(&mbar);
+    if (threadIdx.x == 0) mbar_init(bar, 1);  // nothing ever arrives
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = global_timer_ns();
+        bool done = false;
+        while (!(done = mbar_try_wait(bar, 0))) {
+            if (global_timer_ns() - t0 > (uint64_t)timeout_us * 1000ull) break;
+        }
+        if (!done) atomicExch(status, MLA_ERR_TIMEOUT);
+    }
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+mla_status_t mla_cache_append(const mla_cache_t* cache, const void* ckv_raw, const void* kr_raw, int32_t in_dtype,
+                              const float* gamma, float eps, float rope_base, const int32_t* seq_ids,
+                              const int32_t* positions, int32_t T, uint32_t flags, void* stream) {
+    mla_status_t st = check_cache(cache);
+    if (st != MLA_OK) return st;
+    if (T < 0 || (in_dtype != MLA_BF16 && in_dtype != MLA_FP32)) return MLA_ERR_INVALID_ARG;
+    if (flags & ~(MLA_APPEND_RMSNORM | MLA_APPEND_ROPE)) return MLA_ERR_INVALID_ARG;
+    if (T == 0) return MLA_OK;
+    if (!ckv_raw || (cache->d_r > 0 && !kr_raw) || !seq_ids || !positions) return MLA_ERR_INVALID_ARG;
+    if ((flags & MLA_APPEND_RMSNORM) && !(eps >= 0.f)) return MLA_ERR_INVALID_ARG;
+    if ((flags & MLA_APPEND_ROPE) && !(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+    AppendArgs a;
+    a.seq_ids = seq_ids;
+    a.positions = positions;
+    a.page_table = cache->page_table;
+    a.gamma = gamma;
+    a.T = T;
+    a.num_seqs = cache->num_seqs;
+    a.num_pages = cache->num_pages;
+    a.page_size = cache->page_size;
+    a.max_pages_per_seq = cache->max_pages_per_seq;
+    a.d_c = cache->d_c;
+    a.d_r = cache->d_r;
+    a.flags = flags;
+    a.eps = eps;
+    a.rope_base = rope_base;
+    return cuda_status(launch_append(a, ckv_raw, kr_raw, in_dtype, cache->dtype, cache->data,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+mla_status_t mla_decode(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B, const void* q_nope,
+                        const void* q_rope, int32_t Q, int32_t H, float softmax_scale, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    return run_decode(cache, seq_lens, DecodeShape{B, Q, H, 0}, q_nope, q_rope, softmax_scale, out, lse, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+mla_status_t mla_decode_split_combine(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B,
+                                      const void* q_nope, const void* q_rope, int32_t Q, int32_t H,
+                                      float softmax_scale, int32_t n_split, void* out, float* lse, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    if (n_split < 1 || n_split > kMaxSplit) return MLA_ERR_INVALID_ARG;
+    return run_decode(cache, seq_lens, DecodeShape{B, Q, H, n_split}, q_nope, q_rope, softmax_scale, out, lse,
+                      workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t mla_decode_workspace_size(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t n_split, int32_t num_sms) {
+    if (B < 0 || Q < 1 || H < 1 || d_c < 1 || d_c > 512 || n_split < 0 || n_split > kMaxSplit || num_sms < 0)
+        return 0;
+    if (num_sms == 0) {
+        const DeviceInfo* d = device_info();
+        if (!d || d->err != cudaSuccess) return 0;
+        num_sms = d->sms;
+    }
+    // fp32 path uses one worker per SM, the tensor path fewer: size for the larger
+    return ws_layout(B, Q, H, d_c, n_split, num_sms).total;
+}
+
+mla_status_t mla_decode_plan(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B, int32_t Q, int32_t H,
+                             int32_t n_split, void* workspace, size_t workspace_bytes, void* stream) {
+    mla_status_t st = check_cache(cache);
+    if (st != MLA_OK) return st;
+    if (B < 0 || B > cache->num_seqs || Q < 1 || H < 1 || n_split < 0 || n_split > kMaxSplit)
+        return MLA_ERR_INVALID_ARG;
+    if (B > 0 && !seq_lens) return MLA_ERR_INVALID_ARG;
+    if (B == 0) return MLA_OK;
+    return do_plan(cache, seq_lens, DecodeShape{B, Q, H, n_split}, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream));
+}
+
+mla_status_t mla_decode_attend(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B, const void* q_nope,
+                               const void* q_rope, int32_t Q, int32_t H, float softmax_scale, int32_t n_split,
+                               void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    const DecodeShape s{B, Q, H, n_split};
+    mla_status_t st = check_decode(cache, seq_lens, s, q_nope, q_rope, out);
+    if (st != MLA_OK) return st;
+    return do_attend(cache, seq_lens, s, q_nope, q_rope, softmax_scale, out, lse, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream));
+}
+
+mla_status_t mla_decode_combine(const mla_cache_t* cache, int32_t B, int32_t Q, int32_t H, int32_t n_split, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    mla_status_t st = check_cache(cache);
+    if (st != MLA_OK) return st;
+    if (B < 0 || B > cache->num_seqs || Q < 1 || H < 1 || n_split < 0 || n_split > kMaxSplit)
+        return MLA_ERR_INVALID_ARG;
+    if (B > 0 && !out) return MLA_ERR_INVALID_ARG;
+    return do_combine(cache, DecodeShape{B, Q, H, n_split}, out, lse, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+mla_status_t mla_decode_read_status(void* workspace, size_t workspace_bytes, void* stream, int32_t* status_out) {
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MLA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t code = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemcpy(&code, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+    const int32_t zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
+    if (status_out) *status_out = code;
+    return static_cast<mla_status_t>(code);
+}
+
+mla_status_t mla_selftest_bounded_wait(void* workspace, size_t workspace_bytes, uint32_t timeout_us, void* stream) {
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MLA_ERR_WORKSPACE;
+    if (timeout_us == 0 || timeout_us > 10000000u) return MLA_ERR_INVALID_ARG;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<int*>(workspace), timeout_us);
+    return cuda_status(cudaGetLastError());
+}
+
+const char* mla_status_string(mla_status_t s) {
+    switch (s) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: shape or dtype not supported";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA call failed";
+        case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+        case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        default: return "MLA: unknown status";
+    }
+}
+
+int32_t mla_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,28 @@
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+struct AppendArgs {
+    const int32_t* seq_ids;
+    const int32_t* positions;
+    const int32_t* page_table;
+    const float* gamma;
+    int32_t T;
+    int32_t num_seqs;
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t max_pages_per_seq;
+    int32_t d_c;
+    int32_t d_r;
+    uint32_t flags;
+    float eps;
+    float rope_base;
+};
+
+cudaError_t launch_append(const AppendArgs& a, const void* ckv, const void* kr, int32_t in_dtype,
+                          int32_t cache_dtype, void* cache, cudaStream_t stream);
+
+}  // namespace mla

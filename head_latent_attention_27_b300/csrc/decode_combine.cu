@@ -1,0 +1,86 @@
+// Log-sum-exp merge of the partial rows of units that were split across
+// workers (flash-decoding).  For a row with partial results (o_j, lse_j):
+//     lse = ln sum_j exp(lse_j),   out = sum_j exp(lse_j - lse) o_j
+// Units done by one piece were written by the attention kernel and are
+// skipped; units with no visible key get out = 0 and lse = -inf.
+#include <cuda_bf16.h>
+
+#include "decode_plan.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    combine_kernel(int32_t Q, int32_t H, int32_t d_c, int32_t out_bf16, void* __restrict__ out,
+                   float* __restrict__ lse, void* ws, WsLayout L) {
+    const WsView v = ws_view(ws, L);
+    const int32_t u = blockIdx.x;
+    if (u >= v.hdr->num_units) return;
+    const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t QH = Q * H;
+    const int32_t RB = units_per_seq(Q, H);
+    const int32_t b = u / RB, rb = u % RB;
+    const int32_t row = blockIdx.y * kWarpsPerBlock + warp;
+    const int32_t rows_valid = min(kRowsPerUnit, QH - rb * kRowsPerUnit);
+    if (row >= rows_valid) return;
+    const int32_t p0 = v.unit_piece_begin[u], p1 = v.unit_piece_begin[u + 1];
+    const int32_t n = p1 - p0;
+    if (n == 1) return;
+    const int64_t grow = (int64_t)b * QH + (int64_t)rb * kRowsPerUnit + row;
+
+    float m = -INFINITY;
+    for (int32_t k = 0; k < n; ++k) m = fmaxf(m, v.lse_part[(int64_t)(p0 + k) * kRowsPerUnit + row]);
+    float total_lse = -INFINITY;
+    float z = 0.f;
+    if (m != -INFINITY) {
+        for (int32_t k = 0; k < n; ++k) z += expf(v.lse_part[(int64_t)(p0 + k) * kRowsPerUnit + row] - m);
+        total_lse = m + logf(z);
+    }
+    // out = sum_k w_k o_k with w_k = exp(lse_k - lse)
+    for (int32_t c0 = lane * 4; c0 < d_c; c0 += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (total_lse != -INFINITY) {
+            for (int32_t k = 0; k < n; ++k) {
+                const float lk = v.lse_part[(int64_t)(p0 + k) * kRowsPerUnit + row];
+                if (lk == -INFINITY) continue;
+                const float w = expf(lk - total_lse);
+                const float* src = v.o_part + ((int64_t)(p0 + k) * kRowsPerUnit + row) * d_c + c0;
+                if (c0 + 4 <= d_c) {
+                    const float4 o = *reinterpret_cast<const float4*>(src);
+                    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+                } else {
+                    const int32_t rem = d_c - c0;
+                    acc.x += w * src[0];
+                    if (rem > 1) acc.y += w * src[1];
+                    if (rem > 2) acc.z += w * src[2];
+                }
+            }
+        }
+        const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+        const int32_t cnt = min(4, d_c - c0);
+        if (out_bf16) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + grow * d_c + c0;
+            for (int32_t i = 0; i < cnt; ++i) dst[i] = __float2bfloat16_rn(vals[i]);
+        } else {
+            float* dst = static_cast<float*>(out) + grow * d_c + c0;
+            for (int32_t i = 0; i < cnt; ++i) dst[i] = vals[i];
+        }
+    }
+    if (lse != nullptr && lane == 0) lse[grow] = total_lse;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t out_dtype, void* out,
+                           float* lse, void* ws, const WsLayout& L, cudaStream_t stream) {
+    const int32_t U = B * units_per_seq(Q, H);
+    if (U == 0) return cudaSuccess;
+    const int32_t rows = min(kRowsPerUnit, Q * H);
+    dim3 grid(U, (rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    combine_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(Q, H, d_c, out_dtype == 0, out, lse, ws, L);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

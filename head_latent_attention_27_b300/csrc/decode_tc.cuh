@@ -1,0 +1,41 @@
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "decode_plan.cuh"
+
+namespace mla {
+
+struct TcArgs {
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    void* out;          // bf16 [B*Q*H][512]
+    float* lse;         // [B*Q*H] or null
+    int32_t num_pages;
+    int32_t max_pages_per_seq;
+    int32_t Q;
+    int32_t H;
+    float scale_log2;   // softmax_scale * log2(e)
+    int32_t evict_first;  // stream the cache with an evict-first L2 policy
+};
+
+struct TcMaps {
+    CUtensorMap kv_nope;  // cache [pages*64][576], box 64 x 64, 128-byte swizzle
+    CUtensorMap kv_rope;  // same tensor, box 32 x 64, 64-byte swizzle
+    CUtensorMap q_nope;   // [B*Q*H][512], box 64 x 128, 128-byte swizzle
+    CUtensorMap q_rope;   // [B*Q*H][64], box 32 x 128, 64-byte swizzle
+};
+
+// Dynamic shared memory of the kernel (bytes) and its cluster size.
+size_t decode_tc_smem_bytes();
+constexpr int kTcClusterSize = 2;
+
+// Maximum number of co-resident 2-CTA clusters on the current device.
+cudaError_t decode_tc_max_clusters(int32_t* clusters);
+
+cudaError_t launch_decode_tc(const TcMaps& maps, const TcArgs& a, int32_t num_clusters, void* ws,
+                             const WsLayout& L, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,217 @@
+/*
+ * mla.h -- C ABI of libmla.so: absorbed Multi-head Latent Attention (MLA)
+ * decode over a paged latent cache, hand-written for NVIDIA B300 (sm_103a).
+ *
+ * The operation (page "02 · DeepSeek-V2 analysis", sections 1.2-1.3, 6.1 and
+ * the closing walk of one token through a layer): every token of a layer
+ * caches one row of d_c + d_r elements, the RMSNorm'd latent c^KV (d_c = 512)
+ * followed by one RoPE key k^R (d_r = 64) that all heads share.  With W^UK
+ * absorbed into the query, head h of a query token attends directly over the
+ * cached rows:
+ *
+ *     x_s   = softmax_scale * ( q_nope[h] . c_s  +  q_rope[h] . k^R_s )
+ *     a_s   = softmax_s(x_s)          over the visible history s
+ *     out[h]= sum_s a_s c_s           (in R^{d_c}; W^UV / W^O applied later)
+ *     lse[h]= ln sum_s exp(x_s)
+ *
+ * with softmax_scale = 1/sqrt(d_h + d_h^R) (eq 18: the per-head width of the
+ * concatenated content and RoPE key, not d_c + d_r).
+ *
+ * Conventions shared by all calls
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *    the mla_cache_t descriptor itself and `status_out`, which are host
+ *    pointers read/written during the call only.  The library never
+ *    allocates, frees or synchronises device memory in these calls (except
+ *    mla_decode_read_status, which synchronises the stream it is given).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work on it and returns.
+ *  - Errors are returned, never thrown.  Argument checks that can be done on
+ *    the host return MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED before
+ *    anything is launched.  A launch failure returns MLA_ERR_CUDA.  Checks
+ *    that need device data (sequence lengths, page ids) are done in the
+ *    kernels, which skip the offending work and record MLA_ERR_INVALID_ARG
+ *    in the workspace status word; mla_decode_read_status returns it.
+ *  - Calls are thread-safe.  The only library state is a per-device cache of
+ *    the SM count and kernel attributes.
+ *
+ * Cache layout: data[num_pages][page_size][d_c + d_r], row = [c_kv || k_R].
+ * Token `pos` of sequence `b` lives in page page_table[b][pos / page_size],
+ * slot pos % page_size.  A contiguous cache is the identity page table.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mla_status {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* bad pointer, size, stride or alignment   */
+    MLA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (shape, dtype) */
+    MLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed        */
+    MLA_ERR_TIMEOUT = 4,      /* a bounded in-kernel wait ran out         */
+    MLA_ERR_WORKSPACE = 5     /* workspace missing or too small           */
+} mla_status_t;
+
+typedef enum mla_dtype {
+    MLA_BF16 = 0,             /* bfloat16 */
+    MLA_FP32 = 1              /* IEEE float32 */
+} mla_dtype_t;
+
+/* Describes a paged latent cache.  Plain data; the caller owns both arrays. */
+typedef struct mla_cache {
+    void* data;                /* device [num_pages][page_size][d_c + d_r]          */
+    const int32_t* page_table; /* device int32 [B][max_pages_per_seq], page ids     */
+    int32_t dtype;             /* mla_dtype_t of `data`                             */
+    int32_t num_seqs;          /* rows of page_table (sequences addressable)        */
+    int32_t num_pages;         /* pages in the pool (>= 1)                          */
+    int32_t page_size;         /* tokens per page: must be 64                       */
+    int32_t d_c;               /* latent width: 512 for bf16; 4..512, mult. of 4, fp32 */
+    int32_t d_r;               /* RoPE key width: 64 for bf16, 2..64 (even) fp32    */
+    int32_t max_pages_per_seq; /* row stride of page_table (>= 1)                   */
+} mla_cache_t;
+
+/* flags for mla_cache_append */
+#define MLA_APPEND_RMSNORM 1u  /* c_kv row := RMSNorm(c_kv_raw) * gamma          */
+#define MLA_APPEND_ROPE    2u  /* k_R row  := RoPE(k_R_raw, position)            */
+
+/*
+ * mla_cache_append -- write T new tokens into the cache.
+ * Follows the DeepSeek-V2 analysis page: an RMSNorm after the compressed
+ * latent (section 1.2), the shared key k^R rotated by RoPE at the token's
+ * position and cached (section 1.3, eq 14-15), "the token's 576 elements
+ * join the cache" (walk of one token); RoPE rotates the pairs (2i, 2i+1)
+ * (page "DeepSeek-V3 model structure", section 2(3)).
+ *
+ *  ckv_raw  [T][d_c], kr_raw [T][d_r]: in_dtype (bf16 or fp32), row-major.
+ *  gamma    [d_c] fp32 or NULL (= all ones).  Used with MLA_APPEND_RMSNORM.
+ *  eps      RMSNorm epsilon: y = x / sqrt(mean(x^2) + eps) * gamma.
+ *  rope_base  theta_i = rope_base^(-2i/d_r); angle = position * theta_i;
+ *           (y_2i, y_2i+1) = (x_2i cos - x_2i+1 sin, x_2i sin + x_2i+1 cos).
+ *  seq_ids, positions [T] int32: destination sequence and position.
+ *  Without a flag the corresponding part is copied (converted to the cache
+ *  dtype).  Arithmetic in fp32 (angles in fp64), one rounding to the cache
+ *  dtype (round to nearest even).  Out-of-range seq_id / position / page id
+ *  skip the row (nothing is written); that is not reported.
+ *  Returns MLA_OK, MLA_ERR_INVALID_ARG (NULL pointers, T < 0, bad cache
+ *  descriptor), MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.  T = 0 is a no-op.
+ */
+MLA_API mla_status_t mla_cache_append(const mla_cache_t* cache,
+                              const void* ckv_raw, const void* kr_raw, int32_t in_dtype,
+                              const float* gamma, float eps, float rope_base,
+                              const int32_t* seq_ids, const int32_t* positions, int32_t T,
+                              uint32_t flags, void* stream);
+
+/*
+ * mla_decode -- absorbed MLA attention of Q query tokens per sequence.
+ *
+ *  seq_lens [B] int32 (device): cached tokens of each sequence, INCLUDING
+ *           its Q query tokens (already appended).  Query j (0 <= j < Q) of
+ *           sequence b sits at position seq_lens[b]-Q+j and sees positions
+ *           0..seq_lens[b]-Q+j (causal).  A query that sees no position gets
+ *           out = 0 and lse = -inf.  0 <= seq_lens[b] <= max_pages_per_seq*64.
+ *  q_nope   [B][Q][H][d_c] absorbed content queries, cache dtype.
+ *  q_rope   [B][Q][H][d_r] RoPE queries, already rotated at their position.
+ *  softmax_scale  usually 1/sqrt(d_h + d_h^R).
+ *  out      [B][Q][H][d_c], cache dtype.   lse [B][Q][H] fp32 or NULL.
+ *  workspace / workspace_bytes: device scratch of at least
+ *           mla_decode_workspace_size(B, Q, H, d_c, 0, 0) bytes, 256-byte
+ *           aligned, owned by the caller; its contents are not needed
+ *           between calls.  Calls sharing a workspace must not overlap.
+ *  Shapes: bf16 cache needs d_c = 512, d_r = 64, page_size = 64, Q*H <= 4096,
+ *  16-byte aligned cache/q/out; fp32 cache needs d_c <= 512 (multiple of 4)
+ *  and d_r <= 64 (even).  B <= cache->num_seqs.  The work is split across the
+ *  SMs by a balanced partition of all key tiles (flash-decoding), then
+ *  partial results are merged by log-sum-exp.
+ *  Equivalent to mla_decode_plan(n_split = 0) + mla_decode_attend +
+ *  mla_decode_combine.
+ */
+MLA_API mla_status_t mla_decode(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B,
+                        const void* q_nope, const void* q_rope, int32_t Q, int32_t H,
+                        float softmax_scale, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_split_combine -- same result as mla_decode, but every sequence's
+ * visible keys are cut into n_split (1..1024) equal chunks of whole 64-token
+ * tiles; each chunk yields a partial (fp32 out, lse) and the chunks are merged
+ * by log-sum-exp: lse = ln sum_j exp(lse_j), out = sum_j exp(lse_j - lse) out_j.
+ * Chunks past the end of a short sequence are empty and contribute nothing.
+ * Workspace: mla_decode_workspace_size(B, Q, H, d_c, n_split, 0).
+ */
+MLA_API mla_status_t mla_decode_split_combine(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B,
+                                      const void* q_nope, const void* q_rope, int32_t Q, int32_t H,
+                                      float softmax_scale, int32_t n_split, void* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace needed by a decode of this shape.  n_split = 0 selects
+ * the balanced partition of mla_decode, n_split >= 1 the uniform split of
+ * mla_decode_split_combine.  num_sms = 0 queries the current device.
+ * Returns 0 for invalid arguments.
+ */
+MLA_API size_t mla_decode_workspace_size(int32_t B, int32_t Q, int32_t H, int32_t d_c,
+                                 int32_t n_split, int32_t num_sms);
+
+/*
+ * The three phases of a decode, callable one by one.  The plan depends only
+ * on seq_lens, B, Q, H, n_split and the device, so a caller that decodes
+ * several layers with the same lengths may plan once and attend/combine per
+ * layer.  mla_decode_plan writes the partition of work into `workspace`;
+ * mla_decode_attend runs the attention kernel and writes final rows into
+ * out/lse and partial rows into the workspace; mla_decode_combine merges the
+ * partial rows.  All three take the same workspace and the same n_split
+ * (0 = balanced); the cache dtype selects the kernel (tensor-core path for
+ * bf16, CUDA-core path for fp32).
+ */
+MLA_API mla_status_t mla_decode_plan(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B,
+                             int32_t Q, int32_t H, int32_t n_split,
+                             void* workspace, size_t workspace_bytes, void* stream);
+MLA_API mla_status_t mla_decode_attend(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B,
+                               const void* q_nope, const void* q_rope, int32_t Q, int32_t H,
+                               float softmax_scale, int32_t n_split, void* out, float* lse,
+                               void* workspace, size_t workspace_bytes, void* stream);
+MLA_API mla_status_t mla_decode_combine(const mla_cache_t* cache, int32_t B, int32_t Q, int32_t H,
+                                int32_t n_split, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then returns (and clears) the status word the
+ * kernels of the last decode on `workspace` recorded: MLA_OK,
+ * MLA_ERR_INVALID_ARG (bad sequence length or page id met on the device) or
+ * MLA_ERR_TIMEOUT (a bounded wait ran out; the kernel stopped cleanly).
+ * The code is also stored in *status_out when status_out is not NULL.
+ */
+MLA_API mla_status_t mla_decode_read_status(void* workspace, size_t workspace_bytes, void* stream,
+                                    int32_t* status_out);
+
+/*
+ * Self-test of the bounded wait used by every in-kernel wait: launches one
+ * block that waits on a barrier nothing ever completes, gives up after
+ * `timeout_us` microseconds, records MLA_ERR_TIMEOUT in the workspace status
+ * word and exits.  Lets a test exercise the timeout path without a hang.
+ */
+MLA_API mla_status_t mla_selftest_bounded_wait(void* workspace, size_t workspace_bytes,
+                                       uint32_t timeout_us, void* stream);
+
+/* Static description of a status code. */
+MLA_API const char* mla_status_string(mla_status_t status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+MLA_API int32_t mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

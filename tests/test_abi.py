@@ -1,0 +1,121 @@
+"""The C-ABI library: loads, exports what include/mla.h declares, validates
+arguments on the host.  No kernel is launched here (runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def mla():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("_mla_build", os.path.join(ROOT, "head_latent_attention_27_b300", "build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    b.build()
+    import head_latent_attention_27_b300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mla_cache_append", "mla_decode", "mla_decode_split_combine",
+                     "mla_decode_workspace_size", "mla_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(mla):
+    lib = ctypes.CDLL(mla.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(mla.EXPORTED)
+
+
+def test_status_strings(mla):
+    for code in range(6):
+        assert mla.mla_status_string(code).startswith("MLA_")
+    assert "unknown" in mla.mla_status_string(99)
+
+
+def test_workspace_size_is_host_arithmetic(mla):
+    n0 = mla.mla_decode_workspace_size(64, 1, 128, 512, 0, 148)
+    n32 = mla.mla_decode_workspace_size(4, 1, 128, 512, 32, 148)
+    # balanced: at most units + workers pieces of 128 x 512 fp32 partial rows
+    assert n0 >= (64 + 148) * 128 * 512 * 4
+    assert n32 >= 4 * 32 * 128 * 512 * 4
+    assert mla.mla_decode_workspace_size(64, 2, 128, 512, 0, 148) > n0
+    with pytest.raises(RuntimeError):
+        mla.mla_decode_workspace_size(0, 0, 128, 512, 0, 148)
+    with pytest.raises(RuntimeError):
+        mla.mla_decode_workspace_size(4, 1, 128, 512, 5000, 148)
+
+
+def _cache(mla, **kw):
+    c = dict(data=0x1000, page_table=0x2000, dtype=mla.MLA_BF16, num_seqs=4, num_pages=16, page_size=64,
+             d_c=512, d_r=64, max_pages_per_seq=4)
+    c.update(kw)
+    return mla.mla_cache_t(**c)
+
+
+def _decode(mla, cache, B=2, Q=1, H=128, ws_bytes=1 << 30, seq=0x3000, qn=0x4000, qr=0x5000, out=0x6000,
+            ws=0x100000):
+    return mla._lib.mla_decode(ctypes.byref(cache), seq, B, qn, qr, Q, H, 0.07, out, None, ws, ws_bytes, None)
+
+
+def test_decode_rejects_bad_arguments_before_launch(mla):
+    E = mla
+    assert mla._lib.mla_decode(None, 0x3000, 2, 0x4000, 0x5000, 1, 128, 0.07, 0x6000, None, 0x100000, 1 << 30,
+                               None) == E.MLA_ERR_INVALID_ARG
+    assert _decode(mla, _cache(mla, data=None)) == E.MLA_ERR_INVALID_ARG
+    assert _decode(mla, _cache(mla, page_size=32)) == E.MLA_ERR_UNSUPPORTED
+    assert _decode(mla, _cache(mla, d_c=256)) == E.MLA_ERR_UNSUPPORTED
+    assert _decode(mla, _cache(mla, d_r=63)) == E.MLA_ERR_INVALID_ARG
+    assert _decode(mla, _cache(mla, dtype=7)) == E.MLA_ERR_INVALID_ARG
+    assert _decode(mla, _cache(mla, data=0x1008)) == E.MLA_ERR_INVALID_ARG     # not 16-byte aligned
+    assert _decode(mla, _cache(mla), B=5) == E.MLA_ERR_INVALID_ARG              # B > num_seqs
+    assert _decode(mla, _cache(mla), Q=0) == E.MLA_ERR_INVALID_ARG
+    assert _decode(mla, _cache(mla), H=0) == E.MLA_ERR_INVALID_ARG
+    assert _decode(mla, _cache(mla), Q=64, H=128) == E.MLA_ERR_UNSUPPORTED      # Q*H > 4096
+    assert _decode(mla, _cache(mla), qn=None) == E.MLA_ERR_INVALID_ARG
+    assert _decode(mla, _cache(mla), out=0x6004) == E.MLA_ERR_INVALID_ARG      # misaligned out
+    assert _decode(mla, _cache(mla, dtype=mla.MLA_FP32, d_c=66, d_r=16)) == E.MLA_ERR_UNSUPPORTED
+    assert _decode(mla, _cache(mla, num_pages=0)) == E.MLA_ERR_INVALID_ARG
+    c = _cache(mla)
+    assert mla._lib.mla_decode_split_combine(ctypes.byref(c), 0x3000, 2, 0x4000, 0x5000, 1, 128, 0.07, 0,
+                                             0x6000, None, 0x100000, 1 << 30, None) == E.MLA_ERR_INVALID_ARG
+    assert mla._lib.mla_decode_split_combine(ctypes.byref(c), 0x3000, 2, 0x4000, 0x5000, 1, 128, 0.07, 2000,
+                                             0x6000, None, 0x100000, 1 << 30, None) == E.MLA_ERR_INVALID_ARG
+
+
+def test_append_rejects_bad_arguments_before_launch(mla):
+    c = _cache(mla)
+    f = mla._lib.mla_cache_append
+    ok_args = dict(ckv=0x7000, kr=0x8000, dt=mla.MLA_BF16, seq=0x9000, pos=0xA000, T=4, flags=3)
+
+    def call(**kw):
+        a = dict(ok_args)
+        a.update(kw)
+        return f(ctypes.byref(c), a["ckv"], a["kr"], a["dt"], None, 1e-6, 10000.0, a["seq"], a["pos"], a["T"],
+                 a["flags"], None)
+
+    assert call(T=-1) == mla.MLA_ERR_INVALID_ARG
+    assert call(T=0) == mla.MLA_OK                    # no-op, launches nothing
+    assert call(ckv=None) == mla.MLA_ERR_INVALID_ARG
+    assert call(seq=None) == mla.MLA_ERR_INVALID_ARG
+    assert call(dt=5) == mla.MLA_ERR_INVALID_ARG
+    assert call(flags=8) == mla.MLA_ERR_INVALID_ARG
+    assert f(None, 0x7000, 0x8000, 0, None, 1e-6, 1e4, 0x9000, 0xA000, 4, 3, None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_zero_batch_decode_is_a_no_op(mla):
+    c = _cache(mla)
+    assert _decode(mla, c, B=0, seq=None, qn=None, qr=None, out=None) == mla.MLA_OK

@@ -1,0 +1,190 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from gpu_util import build_cache, compare, mla_pkg, run_decode
+from synth.device import to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _ordered(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> integers ordered like the values (for ulp distance)."""
+    b = bits.astype(np.int32)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+# ------------------------------------------------------------------ append --
+
+def test_append_places_rows_bit_exactly_and_within_one_ulp():
+    w = synth.custom_bf16("append_paged", 501, [1, 63, 64, 65, 130, 257], H=4, paged=True)
+    cache, d = build_cache(w)
+    pool = cache.data.view(torch.int16).cpu().numpy().view(np.uint16)
+    # oracle pool from the same raw draws
+    ref = np.full(pool.shape, np.nan)
+    seq, pos = w.token_seq_pos()
+    c_raw, k_raw = w.all_raw_rows()
+    rows = O.append_rows(O.widen(c_raw, "bf16"), O.widen(k_raw, "bf16"), pos, np.ones(w.d_c), w.eps,
+                         w.rope_base, O.append_flags(w), "bf16")
+    O.cache_write(ref, w.page_table(), seq, pos, rows)
+    written_ref = ~np.isnan(ref[:, :, 0])
+    got_vals = O.bf16_bits_to_f64(pool)
+    written_gpu = ~np.isnan(got_vals[:, :, 0])
+    assert np.array_equal(written_ref, written_gpu)            # placement: bit-exact
+    assert np.all(np.isnan(got_vals[~written_gpu]))            # untouched slots keep the canary
+    ref_bits = O.f64_to_bf16_bits(ref[written_ref])
+    ulp = np.abs(_ordered(pool[written_ref]) - _ordered(ref_bits))
+    assert ulp.max() <= 1, ulp.max()
+    assert np.mean(ulp == 0) > 0.99
+
+
+@pytest.mark.parametrize("positions", [[0, 4095, 4096, 131071]])
+def test_append_rope_at_position_edges(positions):
+    mla = mla_pkg()
+    pages = 131072 // 64
+    perm = synth.permutation(77, 9, pages)
+    pool = torch.full((pages, 64, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pt = torch.from_numpy(perm.reshape(1, pages)).cuda()
+    cache = mla.Cache(pool, pt, 512, 64)
+    T = len(positions)
+    c_raw = synth.normal(5, 1, T * 512, 1 / 24, 0, "bf16").reshape(T, 512)
+    k_raw = synth.normal(5, 2, T * 64, 1 / 24, 0, "bf16").reshape(T, 64)
+    pos = np.array(positions, dtype=np.int32)
+    mla.mla_cache_append(cache, to_torch(c_raw, "bf16"), to_torch(k_raw, "bf16"),
+                         torch.zeros(T, dtype=torch.int32, device="cuda"), torch.from_numpy(pos).cuda())
+    got = pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref = O.append_rows(O.widen(c_raw, "bf16"), O.widen(k_raw, "bf16"), pos, np.ones(512), 1e-6, 10000.0, 3, "bf16")
+    for i, p in enumerate(positions):
+        row = got[perm[p // 64], p % 64]
+        ulp = np.abs(_ordered(row) - _ordered(O.f64_to_bf16_bits(ref[i])))
+        assert ulp.max() <= 1, (p, ulp.max())
+    assert int(np.sum(~np.isnan(O.bf16_bits_to_f64(got[:, :, 0])))) == T
+    # position 0: the RoPE key is copied unchanged
+    assert np.array_equal(got[perm[0], 0, 512:], k_raw[0])
+
+
+# -------------------------------------------------------------- fp32 path --
+
+@pytest.mark.parametrize("n_split", [None, 2, 4, 64])
+def test_tiny_fp32_config_within_1e5(n_split):
+    w = synth.tiny_fp32()
+    cache, d = build_cache(w)
+    out, lse = run_decode(w, cache, d, n_split=n_split)
+    compare(w, out, lse)
+
+
+# -------------------------------------------------------------- bf16 path --
+
+SMALL_CASES = [
+    # name, lens, H, Q, paged, q_gain
+    ("h128_q1_ragged", [1, 2, 63, 64, 65, 127, 128, 129, 300, 1000], 128, 1, True, 1.0),
+    ("h16_q1_ragged", [1, 5, 64, 65, 200, 777], 16, 1, True, 1.0),
+    ("h32_q1", [100, 64, 3000], 32, 1, False, 1.0),
+    ("h64_q2_one_unit", [1, 2, 64, 65, 66, 400], 64, 2, True, 1.0),
+    ("h128_q2_two_units", [1, 2, 3, 64, 65, 66, 500], 128, 2, True, 1.0),
+    ("h16_q2", [1, 2, 129, 1025], 16, 2, True, 1.0),
+    ("h128_sharp_softmax", [50, 700, 2049], 128, 1, True, 16.0),
+    ("h128_q2_sharp", [2, 130, 999], 128, 2, True, 16.0),
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=[c[0] for c in SMALL_CASES])
+def test_bf16_small_cases(case):
+    name, lens, H, Q, paged, q_gain = case
+    w = synth.custom_bf16(name, 600 + len(name), lens, H=H, Q=Q, paged=paged, q_gain=q_gain)
+    cache, d = build_cache(w)
+    out, lse = run_decode(w, cache, d)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("n_split", [1, 3, 32, 200])
+def test_bf16_split_combine_small(n_split):
+    w = synth.custom_bf16("split_small", 701, [1, 65, 640, 1999, 4096], H=128, Q=1, paged=True)
+    cache, d = build_cache(w)
+    out, lse = run_decode(w, cache, d, n_split=n_split)
+    compare(w, out, lse)
+
+
+def test_bf16_three_phases_equal_one_call():
+    w = synth.custom_bf16("phases", 702, [700, 64, 3001, 1], H=128, Q=2, paged=True)
+    cache, d = build_cache(w)
+    out1, lse1 = run_decode(w, cache, d)
+    out2, lse2 = run_decode(w, cache, d, phases=True)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+    compare(w, out1, lse1)
+
+
+def test_bf16_many_short_sequences_more_units_than_workers():
+    lens = synth.uniform_int(703, 5, 300, 1, 300)
+    w = synth.custom_bf16("many_short", 703, lens, H=128, Q=1, paged=True)
+    cache, d = build_cache(w)
+    out, lse = run_decode(w, cache, d)
+    compare(w, out, lse, seqs=range(0, 300, 7))
+
+
+def test_bad_sequence_length_is_reported_not_faulted():
+    mla = mla_pkg()
+    w = synth.custom_bf16("bad_len", 704, [64, 128], H=128, Q=1)
+    cache, d = build_cache(w)
+    d["seq_lens"][1] = 10 ** 6          # beyond the page table's capacity
+    out = torch.empty((2, 1, 128, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((2, 1, 128), dtype=torch.float32, device="cuda")
+    ws = mla.alloc_workspace(2, 1, 128)
+    mla.mla_decode(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, lse=lse, workspace=ws)
+    assert mla.mla_decode_read_status(ws) == mla.MLA_ERR_INVALID_ARG
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    mla = mla_pkg()
+    ws = mla.alloc_workspace(1, 1, 128)
+    ws.zero_()
+    mla.mla_selftest_bounded_wait(ws, timeout_us=20000)
+    assert mla.mla_decode_read_status(ws) == mla.MLA_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    assert float(torch.ones(4, device="cuda").sum()) == 4.0
+
+
+# ------------------------------------------------- full-size, sampled rows --
+
+def _sample(w, k=3):
+    idx = {0, w.B // 2, w.B - 1, int(np.argmax(w.lens)), int(np.argmin(w.lens))}
+    return sorted(idx)[: max(k, 3) + 2]
+
+
+def test_full_small_head_config():
+    w = synth.small_head()
+    cache, d = build_cache(w)
+    out, lse = run_decode(w, cache, d)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    compare(w, out, lse, seqs=_sample(w))
+
+
+def test_full_width_config():
+    w = synth.full_width()
+    cache, d = build_cache(w)
+    out, lse = run_decode(w, cache, d)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    compare(w, out, lse, seqs=_sample(w))
+
+
+def test_full_ragged_paged_q2_config():
+    w = synth.ragged_paged()
+    cache, d = build_cache(w)
+    out, lse = run_decode(w, cache, d)
+    assert np.all(np.isfinite(out))
+    compare(w, out, lse, seqs=_sample(w))
+
+
+@pytest.mark.parametrize("n_split", [32, 64, 128])
+def test_full_long_split_config(n_split):
+    w = synth.long_split()
+    cache, d = build_cache(w)
+    out, lse = run_decode(w, cache, d, n_split=n_split)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    compare(w, out, lse, seqs=[0, 3])
