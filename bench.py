@@ -1,0 +1,435 @@
+"""Benchmark of the absorbed MLA decode step on B300.
+
+One step = append the B*Q new tokens' rows (RMSNorm + RoPE + paged write)
++ decode all B sequences (plan, attend, combine), on the full-width workload
+B=64, S=4096, H=128, d_c=512, d_r=64, bf16, one query token per sequence.
+Inputs are seeded synthetic draws resident in HBM before timing starts.
+
+Prints one JSON line.  `value` = decode tokens/s (B*Q query tokens per
+step) over all ranks; the attention kernel's roofline fraction, the e2e
+figure through host buffers and the fp64 oracle's CPU throughput are
+reported alongside.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode tokens/s, cache-read GB/s and TFLOP/s vs B300 roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_counts(w):
+    """Bytes the method must move and flops it must do (per decode)."""
+    import numpy as np
+    elt = 2 if w.dtype == "bf16" else 4
+    width = w.d_c + w.d_r
+    cache_bytes = int(np.sum(w.lens.astype(np.int64))) * width * elt
+    q_bytes = w.B * w.Q * w.H * width * elt
+    out_bytes = w.B * w.Q * w.H * w.d_c * elt
+    visible = 0
+    for b in range(w.B):
+        for j in range(w.Q):
+            visible += max(0, int(w.lens[b]) - w.Q + j + 1)
+    flops = 2 * w.H * (width + w.d_c) * visible
+    return cache_bytes + q_bytes + out_bytes, flops, cache_bytes
+
+
+def kernel_traffic(profile_name: str, src_file: str):
+    """ncu DRAM bytes per launch from the committed summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{16,64})", text)
+    if not m or not h:
+        return None
+    with open(os.path.join(ROOT, src_file), "rb") as f:
+        cur = hashlib.sha256(f.read()).hexdigest()
+    if not cur.startswith(h.group(1)):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ oracle --
+
+class OracleStep:
+    """The fp64 oracle on the host cores over sampled sequences of the
+    workload.  The history cache (all but the newest Q tokens) is built once;
+    a step appends each sampled sequence's newest tokens and decodes it."""
+
+    def __init__(self, w, seqs):
+        import numpy as np
+        import oracle as O
+        self.w, self.seqs, self.O, self.np = w, list(seqs), O, np
+        self.caches = {b: O.sequence_cache(w, b, 0, int(w.lens[b]) - w.Q) for b in self.seqs}
+        self.raw_new = {b: w.raw_rows(b, int(w.lens[b]) - w.Q, int(w.lens[b])) for b in self.seqs}
+        try:
+            from threadpoolctl import threadpool_info
+            self.cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        except Exception:  # pragma: no cover
+            self.cores = os.cpu_count() or 1
+
+    def run(self) -> int:
+        w, O, np = self.w, self.O, self.np
+        for b in self.seqs:
+            c_raw, k_raw = self.raw_new[b]
+            L = int(w.lens[b])
+            rows = O.append_rows(O.widen(c_raw, w.raw_dtype), O.widen(k_raw, w.raw_dtype), np.arange(L - w.Q, L),
+                                 np.ones(w.d_c), w.eps, w.rope_base, O.append_flags(w), w.dtype)
+            C = np.concatenate([self.caches[b][0], rows[:, :w.d_c]])
+            R = np.concatenate([self.caches[b][1], rows[:, w.d_c:]])
+            O.decode_sequence(w, b, cache=(C, R))
+        return len(self.seqs) * w.Q
+
+
+def oracle_throughput(w, seqs, budget_s: float = 10.0):
+    """Tokens/s of the oracle, repeating steps for about `budget_s` seconds."""
+    st = OracleStep(w, seqs)
+    t0 = time.perf_counter()
+    tokens, passes = 0, 0
+    while True:
+        tokens += st.run()
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return tokens / el, st.cores, el, passes
+
+
+def run_reference(args, w):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    seqs = list(range(min(4, w.B)))
+    st = OracleStep(w, seqs)
+    for _ in range(args.warmup):
+        st.run()
+    t0 = time.perf_counter()
+    tokens = 0
+    for _ in range(args.steps):
+        tokens += st.run()
+    el = time.perf_counter() - t0
+    value = tokens / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "S": int(w.lens[0]), "H": w.H, "Q": w.Q, "d_c": w.d_c,
+                   "d_r": w.d_r},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": st.cores, "kind": "oracle",
+                         "sample": f"sequences {seqs} of the workload per step (newest token appended + decoded)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- CUDA arm --
+
+def run_cuda(args, w):
+    import numpy as np
+    import torch
+
+    import head_latent_attention_27_b300 as mla
+    from synth.device import empty_pool, to_torch, upload
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # ---- resident inputs: cache built by the append kernel from raw rows
+    d = upload(w, dev)
+    pool = empty_pool(w, dev, fill_nan=False)
+    cache = mla.Cache(pool, d["page_table"], w.d_c, w.d_r)
+    flags = mla.MLA_APPEND_RMSNORM | mla.MLA_APPEND_ROPE
+    mla.mla_cache_append(cache, d["raw_c"], d["raw_k"], d["seq_ids"], d["positions"], eps=w.eps,
+                         rope_base=w.rope_base, flags=flags)
+    # the step's new rows: the last Q tokens of every sequence
+    last = np.concatenate([w.row_offset[b] + np.arange(int(w.lens[b]) - w.Q, int(w.lens[b])) for b in range(w.B)])
+    new_c = d["raw_c"][torch.from_numpy(last).to(dev)].contiguous()
+    new_k = d["raw_k"][torch.from_numpy(last).to(dev)].contiguous()
+    new_seq = d["seq_ids"][torch.from_numpy(last).to(dev)].contiguous()
+    new_pos = d["positions"][torch.from_numpy(last).to(dev)].contiguous()
+    del d["raw_c"], d["raw_k"]
+    out = torch.empty((w.B, w.Q, w.H, w.d_c), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Q, w.H), dtype=torch.float32, device=dev)
+    ws = mla.alloc_workspace(w.B, w.Q, w.H, w.d_c, 0, dev)
+    scale = 1.0 / math.sqrt(w.d_h + w.d_r)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # The step's launches are captured once in CUDA graphs (append+plan,
+    # attend, combine) so that host launch overhead does not starve the GPU;
+    # the event pairs bracket the replays on the same stream.
+    def pre():
+        mla.mla_cache_append(cache, new_c, new_k, new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
+        mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws)
+
+    def attend():
+        mla.mla_decode_attend(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, ws, lse=lse, softmax_scale=scale)
+
+    def post():
+        mla.mla_decode_combine(cache, out, ws, lse=lse)
+
+    launches_per_step = 4  # append, plan, attend, combine
+
+    for _ in range(args.warmup):    # eager warm-up (also initialises the library)
+        pre(); attend(); post()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    status = mla.mla_decode_read_status(ws)
+    if status != mla.MLA_OK:
+        raise RuntimeError(f"kernel status {mla.mla_status_string(status)}")
+    graphs = []
+    for fn in (pre, attend, post):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    g_pre, g_att, g_post = graphs
+    for _ in range(args.warmup):
+        g_pre.replay(); g_att.replay(); g_post.replay()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            g_pre.replay()
+            ev_att[i][0].record(stream)
+            g_att.replay()
+            ev_att[i][1].record(stream)
+            g_post.replay()
+            ev[i][1].record(stream)
+            flush.zero_()          # L2 flush between steps, outside the event pairs
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        t_wall = time.perf_counter() - t_wall0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    att_ms = [a.elapsed_time(b) for a, b in ev_att]
+    tot_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    status = mla.mla_decode_read_status(ws)
+    if status != mla.MLA_OK:
+        raise RuntimeError(f"kernel status {mla.mla_status_string(status)}")
+
+    # ---- e2e through the public API with host buffers (pinned), per step:
+    #      H2D of the step's queries and new raw rows, append+decode, D2H of out and lse
+    h_qn = d["q_nope"].cpu().pin_memory()
+    h_qr = d["q_rope"].cpu().pin_memory()
+    h_c = new_c.cpu().pin_memory()
+    h_k = new_k.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_qn, d_qr = torch.empty_like(d["q_nope"]), torch.empty_like(d["q_rope"])
+    d_c, d_k = torch.empty_like(new_c), torch.empty_like(new_k)
+    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qr, h_c, h_k))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        d_qn.copy_(h_qn, non_blocking=True)
+        d_qr.copy_(h_qr, non_blocking=True)
+        d_c.copy_(h_c, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        mla.mla_cache_append(cache, d_c, d_k, new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
+        mla.mla_decode(cache, d["seq_lens"], d_qn, d_qr, out, lse=lse, workspace=ws, softmax_scale=scale)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e):
+        e2e_step()
+    for _ in range(args.warmup):
+        g_e2e.replay()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g_e2e.replay()
+        b.record(stream)
+        flush.zero_()
+        e2e_ms.append((a, b))
+    torch.cuda.synchronize(dev)
+    e2e_tot = sum(a.elapsed_time(b) for a, b in e2e_ms)
+    if dist is not None:
+        t = torch.tensor([e2e_tot], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_tot = float(t.item())
+
+    if rank == 0:
+        peaks, peak_kind = load_peaks()
+        alg_bytes, flops, cache_bytes = algorithmic_counts(w)
+        att_avg_s = statistics.mean(att_ms) * 1e-3
+        step_s = tot_ms * 1e-3 / args.steps
+        tokens_per_step = w.B * w.Q
+        value = world * tokens_per_step / step_s
+        hbm = peaks["hbm_gbs"]
+        tc_peak = peaks["bf16_tflops"]
+        t_mem = alg_bytes / (hbm * 1e9)
+        t_tc = flops / (tc_peak * 1e12)
+        bound = "hbm" if t_mem >= t_tc else "tensor"
+        achieved_gbs = alg_bytes / att_avg_s / 1e9
+        achieved_tf = flops / att_avg_s / 1e12
+        traffic = kernel_traffic("decode_tc_full_width.md", "head_latent_attention_27_b300/csrc/decode_tc.cu")
+        if bound == "hbm":
+            roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved_gbs / hbm, "traffic": traffic}
+        else:
+            roof = {"bound": "tensor", "achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": achieved_tf / tc_peak, "traffic": traffic}
+        roof.update({"kernel": "decode_tc_kernel (mla_decode_attend)", "peak_source": f"{peak_kind} burst",
+                     "kernel_ms": att_avg_s * 1e3, "alg_bytes": alg_bytes, "alg_flops": flops,
+                     "roofline_ms": max(t_mem, t_tc) * 1e3, "frac_of_roofline": max(t_mem, t_tc) / att_avg_s,
+                     "tensor_frac": achieved_tf / tc_peak})
+        seqs = list(range(w.B))
+        cpu_v, cores, cpu_el, cpu_steps = oracle_throughput(w, seqs, budget_s=10.0)
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "S": int(w.lens[0]), "H": w.H, "Q": w.Q, "d_c": w.d_c,
+                       "d_r": w.d_r, "page_size": 64, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "l2": "flushed between steps (write > 2x L2 outside the per-step event pairs); "
+                             "cache 302 MB > L2"},
+            "cache_read_gbs": cache_bytes / step_s / 1e9,
+            "tflops": flops / step_s / 1e12,
+            "step_roofline_frac": max(t_mem, t_tc) / step_s,
+            "roofline": roof,
+            "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"all {w.B} sequences, newest token appended + decoded, "
+                                       f"{cpu_steps} pass(es) in {cpu_el:.1f} s"},
+            "e2e": {"value": world * tokens_per_step / (e2e_tot * 1e-3 / args.steps), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "cuda":
+        args.warmup = 3
+    import synth
+    w = synth.full_width()
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_cuda(args, w)
+
+
+if __name__ == "__main__":
+    main()
