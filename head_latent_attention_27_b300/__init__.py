@@ -56,6 +56,7 @@ _SIGS = {
     "mla_decode_combine": (_i32, [_pc, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "mla_decode_read_status": (_i32, [_vp, _sz, _vp, ctypes.POINTER(_i32)]),
     "mla_selftest_bounded_wait": (_i32, [_vp, _sz, _u32, _vp]),
+    "mla_decode_noalloc": (_i32, [_pc, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp]),
     "mla_status_string": (ctypes.c_char_p, [_i32]),
     "mla_version": (_i32, []),
 }
@@ -237,6 +238,17 @@ def mla_decode_combine(cache: Cache, out, workspace, lse=None, n_split: int = 0,
     cc = cache.c()
     _check(_lib.mla_decode_combine(ctypes.byref(cc), B, Q, H, int(n_split), _ptr(out), _ptr(lse), _ptr(workspace),
                                    workspace.numel(), _stream(stream)), "mla_decode_combine")
+
+
+def mla_decode_noalloc(cache: Cache, seq_lens, q_nope, q_rope, out, lse=None,
+                       softmax_scale: float | None = None, d_h: int = 128, stream=None) -> None:
+    """mla_decode without a workspace: the library's fixed scratch array is used
+    (for callers that cannot allocate device memory; calls must not overlap)."""
+    B, Q, H = _decode_args(cache, seq_lens, q_nope, q_rope, out, lse)
+    scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(d_h + cache.d_r)
+    cc = cache.c()
+    _check(_lib.mla_decode_noalloc(ctypes.byref(cc), _ptr(seq_lens), B, _ptr(q_nope), _ptr(q_rope), Q, H,
+                                   float(scale), _ptr(out), _ptr(lse), _stream(stream)), "mla_decode_noalloc")
 
 
 def mla_decode_read_status(workspace, stream=None) -> int:

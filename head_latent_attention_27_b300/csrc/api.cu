@@ -234,6 +234,15 @@ __global__ void selftest_wait_kernel(int* status, uint32_t timeout_us) {
 }
 
 }  // namespace
+
+// Decode (balanced plan) into a given workspace; used by the fixed-scratch
+// entry point in noalloc.cu.  Same checks and launches as mla_decode.
+mla_status_t decode_into_workspace(const mla_cache_t* c, const int32_t* seq_lens, int32_t B, const void* q_nope,
+                                   const void* q_rope, int32_t Q, int32_t H, float scale, void* out, float* lse,
+                                   void* ws, size_t ws_bytes, cudaStream_t stream) {
+    return run_decode(c, seq_lens, DecodeShape{B, Q, H, 0}, q_nope, q_rope, scale, out, lse, ws, ws_bytes, stream);
+}
+
 }  // namespace mla
 
 using namespace mla;

@@ -204,6 +204,36 @@ MLA_API mla_status_t mla_decode_read_status(void* workspace, size_t workspace_by
 MLA_API mla_status_t mla_selftest_bounded_wait(void* workspace, size_t workspace_bytes,
                                        uint32_t timeout_us, void* stream);
 
+/*
+ * mla_decode_noalloc -- mla_decode for callers that cannot give the library
+ * any device memory of its own (no workspace argument).  The pages have no
+ * counterpart to this entry point; it exists for integration only.
+ *
+ * Callers such as a plugin that only receives its input and output buffers
+ * from a host framework, or a serving loop that forbids device allocation
+ * after start-up, cannot call cudaMalloc.  This entry point runs exactly the
+ * decode of mla_decode (same arguments minus the workspace, same results)
+ * using a fixed scratch array of MLA_NOALLOC_SCRATCH_BYTES compiled into the
+ * library: it calls no allocator.  Every GPU that loads the library holds the
+ * array until the process exits.
+ *  - Returns MLA_ERR_WORKSPACE, launching nothing, when the decode needs more
+ *    scratch than MLA_NOALLOC_SCRATCH_BYTES, i.e. more than
+ *    mla_decode_workspace_size(B, Q, H, d_c, 0, clusters) bytes.  On a
+ *    148-SM B300 that allows up to 117 units on the bf16 path and 43 on the
+ *    fp32 path (a unit is one sequence x up to 128 query rows j*H+h, so
+ *    B = 117 sequences at H = 128, Q = 1).
+ *  - All calls on a device share the array; each call rewrites what it reads,
+ *    but calls that overlap on the GPU race and must be serialised.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Device-side problems (bad lengths, page ids) give zero rows as in
+ *    mla_decode; their status word is internal and not reported here.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (48u << 20)
+MLA_API mla_status_t mla_decode_noalloc(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B,
+                                        const void* q_nope, const void* q_rope, int32_t Q, int32_t H,
+                                        float softmax_scale, void* out, float* lse, void* stream);
+
 /* Static description of a status code. */
 MLA_API const char* mla_status_string(mla_status_t status);
 
