@@ -174,7 +174,6 @@ mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShap
     const uint64_t qrows = (uint64_t)s.B * s.Q * s.H;
     if (!encode_2d(&maps.kv_nope, c->data, cache_rows, 576, 576, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&maps.kv_rope, c->data, cache_rows, 576, 576, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !encode_2d(&maps.q_nope, q_nope, qrows, 512, 512, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&maps.q_rope, q_rope, qrows, 64, 64, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
         return MLA_ERR_CUDA;
     TcArgs a;
@@ -188,6 +187,8 @@ mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShap
     a.H = s.H;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.evict_first = units_per_seq(s.Q, s.H) == 1 ? 1 : 0;
+    a.q_nope = q_nope;
+    a.total_rows = (int64_t)qrows;
     return cuda_status(launch_decode_tc(maps, a, P, ws, L, stream));
 }
 

@@ -11,6 +11,7 @@ namespace mla {
 struct TcArgs {
     const int32_t* page_table;
     const int32_t* seq_lens;
+    const void* q_nope;  // bf16 [B*Q*H][512]
     void* out;          // bf16 [B*Q*H][512]
     float* lse;         // [B*Q*H] or null
     int32_t num_pages;
@@ -19,12 +20,12 @@ struct TcArgs {
     int32_t H;
     float scale_log2;   // softmax_scale * log2(e)
     int32_t evict_first;  // stream the cache with an evict-first L2 policy
+    int64_t total_rows;   // B*Q*H
 };
 
 struct TcMaps {
     CUtensorMap kv_nope;  // cache [pages*64][576], box 64 x 64, 128-byte swizzle
     CUtensorMap kv_rope;  // same tensor, box 32 x 64, 64-byte swizzle
-    CUtensorMap q_nope;   // [B*Q*H][512], box 64 x 128, 128-byte swizzle
     CUtensorMap q_rope;   // [B*Q*H][64], box 32 x 128, 64-byte swizzle
 };
 
