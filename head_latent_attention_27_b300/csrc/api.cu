@@ -120,6 +120,10 @@ mla_status_t check_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeS
     return MLA_OK;
 }
 
+// The softmax scale must be a positive finite number (the kernels take the
+// running maximum on unscaled scores).
+bool check_scale(float scale) { return scale > 0.f && isfinite(scale); }
+
 mla_status_t check_workspace(void* ws, size_t bytes, const WsLayout& L) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MLA_ERR_WORKSPACE;
     if (bytes < L.total) return MLA_ERR_WORKSPACE;
@@ -188,6 +192,8 @@ mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShap
     a.scale_log2 = scale * 1.4426950408889634f;
     a.evict_first = units_per_seq(s.Q, s.H) == 1 ? 1 : 0;
     a.q_nope = q_nope;
+    a.cache = c->data;
+    a.prefetch_tiles = kTcPrefetchTiles;
     a.total_rows = (int64_t)qrows;
     return cuda_status(launch_decode_tc(maps, a, P, ws, L, stream));
 }
@@ -209,6 +215,7 @@ mla_status_t run_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeSha
                         cudaStream_t stream) {
     mla_status_t st = check_decode(c, seq_lens, s, q_nope, q_rope, out);
     if (st != MLA_OK) return st;
+    if (!check_scale(scale)) return MLA_ERR_INVALID_ARG;
     if (s.B == 0) return MLA_OK;
     st = do_plan(c, seq_lens, s, ws, ws_bytes, stream);
     if (st != MLA_OK) return st;
@@ -326,6 +333,7 @@ mla_status_t mla_decode_attend(const mla_cache_t* cache, const int32_t* seq_lens
     const DecodeShape s{B, Q, H, n_split};
     mla_status_t st = check_decode(cache, seq_lens, s, q_nope, q_rope, out);
     if (st != MLA_OK) return st;
+    if (!check_scale(softmax_scale)) return MLA_ERR_INVALID_ARG;
     return do_attend(cache, seq_lens, s, q_nope, q_rope, softmax_scale, out, lse, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream));
 }

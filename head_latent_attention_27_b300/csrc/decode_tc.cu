@@ -23,13 +23,17 @@
 // Each accumulates its 256 output columns O += P V with P (bf16) in smem and
 // the same cache tile read as an MN-major V operand.
 //
-// Pipeline (per CTA, 320 threads):
+// Pipeline (per CTA, 448 threads):
 //   warp 0      TMA producer: q_rope per piece, 4-stage ring of cache tiles
 //   warp 1      MMA issuer (owns TMEM); QK runs two tiles ahead of PV so the
 //               score swap of tile g+1 overlaps the softmax of tile g
-//   warps 2-5   softmax: add the peer's half, online softmax (one thread per
-//               row), P -> smem, lazy O rescale, epilogue; q_nope -> TMEM
-//   warps 6-9   score swap: S(g) from TMEM -> fp16 -> st.async to the peer
+//   warps 2-9   softmax, two warpgroups on the same rows: each adds the
+//               peer's half, takes the row max over all 64 columns, and
+//               exponentiates / stores P for its own 32 columns; lazy O
+//               rescale and epilogue split by O columns; q_nope -> TMEM
+//   warps 10-13 score swap: S(g) from TMEM -> fp16 -> st.async to the peer;
+//               one thread forwards "scores read" to the peer (the remote
+//               arrive is slow, so it stays off the softmax warps)
 // TMEM: O 256 columns | q_nope 128 | S double buffer 2 x 64.
 //
 // Every wait is bounded (ptx.cuh: bounded_wait); on a timeout the kernel
@@ -48,7 +52,9 @@ namespace {
 constexpr int BM = 128;          // query rows per unit
 constexpr int BN = 64;           // tokens per tile (= page)
 constexpr int NSTAGE = 4;        // cache-tile ring depth
-constexpr int kThreads = 320;
+constexpr int kSoftmaxWarps = 8;  // two warpgroups
+constexpr int kSwapWarps = 4;
+constexpr int kThreads = 32 * (2 + kSoftmaxWarps + kSwapWarps);   // 448
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_QR = 0;                               // 32 RoPE dims x 128 rows, 64B swizzle
@@ -62,7 +68,8 @@ constexpr uint32_t OFF_P = OFF_KV + NSTAGE * STAGE_BYTES;
 constexpr uint32_t X_BYTES = BM * BN * 2;                    // peer's fp16 partial scores
 constexpr uint32_t OFF_X = OFF_P + 2 * P_BYTES;
 constexpr uint32_t OFF_BAR = OFF_X + 2 * X_BYTES;
-constexpr uint32_t SMEM_USED = OFF_BAR + 256;
+constexpr uint32_t OFF_RED = OFF_BAR + 256;                   // [2 groups][128 rows] fp32 row sums
+constexpr uint32_t SMEM_USED = OFF_RED + 2 * BM * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;            // + alignment slack
 
 static_assert(OFF_KV % 1024 == 0 && STAGE_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_X % 1024 == 0,
@@ -83,11 +90,13 @@ enum : int {
     B_PFULL = B_PEERFREE + 2,       // [2]
     B_PVDONE = B_PFULL + 2,         // [2]
     B_EXIT = B_PVDONE + 2,
-    NUM_BARS
+    B_LRED,                         // [4] row-sum swap of the two softmax warps sharing a lane quarter
+    B_XREAD = B_LRED + 4,           // [2] this CTA's softmax warps are done reading the peer's scores
+    NUM_BARS = B_XREAD + 2
 };
-static_assert(NUM_BARS * 8 <= 192, "barrier area");
-constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 192;
-constexpr uint32_t OFF_ABORT = OFF_BAR + 196;
+static_assert(NUM_BARS * 8 <= 240, "barrier area");
+constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 240;
+constexpr uint32_t OFF_ABORT = OFF_BAR + 244;
 
 // TMEM columns
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384, TM_COLS = 512;
@@ -106,6 +115,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     const __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 2^x on the SFU, flush-to-zero (inputs here are <= 0 or -inf; results
+// below 2^-126 only feed the bf16 probabilities and their sum).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// P = 2^(s*scale_log2 - m) for the 32 columns [C0, C0+32) of a row, packed
+// to bf16 pairs; returns their fp32 sum.  (Compile-time column offset keeps
+// the score array in registers.)
+template <int C0>
+__device__ __forceinline__ float exp_half(const float (&s)[BN], float scale_log2, float neg_mref,
+                                          uint32_t (&pk)[BN / 4]) {
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < BN / 2; c += 2) {
+        const float p0 = fast_exp2(fmaf(s[C0 + c], scale_log2, neg_mref));   // exp2(-inf) = 0
+        const float p1 = fast_exp2(fmaf(s[C0 + c + 1], scale_log2, neg_mref));
+        ls[(c >> 1) & 3] += p0 + p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+    }
+    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
 __device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
@@ -179,20 +213,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(B_QRFULL), 1);
         mbar_init(bar(B_QREMPTY), 1);
-        mbar_init(bar(B_QNFULL), 128);
+        mbar_init(bar(B_QNFULL), kSoftmaxWarps);
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(bar(B_KVFULL + s), 1);
             mbar_init(bar(B_KVEMPTY + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_SFULL + s), 1);
-            mbar_init(bar(B_SEMPTY + s), 256);
+            mbar_init(bar(B_SEMPTY + s), kSoftmaxWarps + kSwapWarps);
             mbar_init(bar(B_XFULL + s), 1);
-            mbar_init(bar(B_PEERFREE + s), 128);
-            mbar_init(bar(B_PFULL + s), 128);
+            mbar_init(bar(B_PEERFREE + s), 1);
+            mbar_init(bar(B_XREAD + s), kSoftmaxWarps);
+            mbar_init(bar(B_PFULL + s), kSoftmaxWarps);
             mbar_init(bar(B_PVDONE + s), 1);
         }
         mbar_init(bar(B_EXIT), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(B_LRED + q), 2);
         *abort_flag = 0;
         fence_mbar_init_cluster();
     }
@@ -224,6 +260,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, q_cnt = 0;
             uint32_t issued_mask = 0, last_parity = 0;
             bool ok = true;
+            // L2 prefetch `prefetch_tiles` tiles ahead of the loads; rank r
+            // prefetches tokens [32r, 32r+32) of a page (one contiguous half),
+            // so the pair covers whole pages.
+            TileCursor pf;
+            pf.init(v.pieces, p_begin, p_end);
+            const uint8_t* cache_bytes = static_cast<const uint8_t*>(a.cache);
+            auto prefetch_next = [&]() {
+                if (!pf.valid()) return;
+                const int32_t pb = pf.pc.unit / RB;
+                const int32_t page = a.page_table[(int64_t)pb * a.max_pages_per_seq + pf.t];
+                if (page >= 0 && page < a.num_pages)
+                    bulk_prefetch_l2(cache_bytes + (int64_t)page * (BN * 1152) + rank * (BN * 576), BN * 576);
+                pf.next();
+            };
+            for (int32_t i = 0; i < a.prefetch_tiles; ++i) prefetch_next();
             for (int32_t p = p_begin; p < p_end && ok; ++p) {
                 const Piece pc = v.pieces[p];
                 const int32_t b = pc.unit / RB, rb = pc.unit % RB;
@@ -238,6 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         atomicCAS(status, 0, 1);
                         page = 0;
                     }
+                    prefetch_next();
                     ok = bounded_wait(bar(B_KVEMPTY + stage), phase ^ 1u, abort_flag, status);
                     if (!ok) break;
                     const uint32_t fb = bar(B_KVFULL + stage);
@@ -334,28 +386,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             umma_commit(bar(B_EXIT));
             drain_wait(bar(B_EXIT), 0);
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + kSoftmaxWarps) {
         // ------------------------------------- softmax / correction / epilogue
+        // Two warpgroups; both hold the same 128 rows (one thread per row and
+        // group).  Each computes the row maximum over all 64 columns of the
+        // tile (so both take identical rescale decisions without talking to
+        // each other), but exponentiates only its own half of the columns,
+        // rescales and stores only its own half of the 256 O columns.
+        const uint32_t half = (uint32_t)((warp - 2) >> 2);
         const uint32_t quarter = (uint32_t)(warp & 3);
         const int32_t row = (int32_t)(quarter * 32 + lane);
         const uint32_t lane_off = (quarter * 32u) << 16;
-        const uint32_t tO = tmem + TM_O + lane_off, tQ = tmem + TM_Q + lane_off;
-        const uint32_t peerfree_remote0 = map_to_cta(bar(B_PEERFREE), peer);
+        const uint32_t tO = tmem + TM_O + lane_off + 128u * half;
+        const uint32_t tQ = tmem + TM_Q + lane_off + 64u * half;
         const bool leader = (threadIdx.x == 64);
         const int rsw = row & 7;
+        float* red = reinterpret_cast<float*>(smem + OFF_RED);
         bool ok = true;
 
-        // q_nope columns of this rank for piece `pp` -> TMEM (A operand of QK)
+        // this group's half of q_nope (128 of the rank's 256 dims) for piece
+        // `pp` -> TMEM (A operand of QK)
         auto write_q = [&](int32_t pp) {
             const Piece pc = v.pieces[pp];
             const int32_t b = pc.unit / RB, rb = pc.unit % RB;
             const int32_t rows_valid = min(BM, QH - rb * BM);
             const int64_t grow = (int64_t)b * QH + rb * BM + row;
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_nope) +
-                                                              grow * 512 + 256 * rank);
+                                                              grow * 512 + 256 * rank + 128 * half);
             const bool have = row < rows_valid;
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t r0[16], r1[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -369,14 +429,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(B_QNFULL));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_QNFULL));
         };
 
         TileCursor cur;
         cur.init(v.pieces, p_begin, p_end);
         if (cur.valid()) write_q(cur.p);
-        uint32_t g = 0;
-        int32_t b = 0, rb = 0, rows_valid = 0, vis = 0, vis_max = 0, qrow = 0;
+        uint32_t g = 0, n_epi = 0;
+        int32_t b = 0, rb = 0, rows_valid = 0, vis = 0, vis_lo = 0, vis_hi = 0, qrow = 0;
         float m_ref = -INFINITY, l = 0.f;
         while (ok && cur.valid()) {
             const uint32_t slot = g & 1u, ph = (g >> 1) & 1u;
@@ -387,27 +448,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 rows_valid = min(BM, QH - rb * BM);
                 qrow = rb * BM + row;
                 vis = row < rows_valid ? visible_len(len, a.Q, a.H, qrow) : 0;
-                vis_max = visible_len(len, a.Q, a.H, rb * BM + rows_valid - 1);
+                vis_lo = visible_len(len, a.Q, a.H, rb * BM);                    // fewest keys of the unit
+                vis_hi = visible_len(len, a.Q, a.H, rb * BM + rows_valid - 1);   // most keys of the unit
                 m_ref = -INFINITY;
                 l = 0.f;
             }
-            // 1. own partial S of tile g
+            // 1. own partial S of tile g (all 64 columns)
             ok = warp_wait(bar(B_SFULL + slot), ph, abort_flag, status);
             if (!ok) break;
             tc_fence_after();
             float s[BN];
             {
-                uint32_t r[32];
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem + TM_S + 64u * slot + lane_off, r0);
+                tmem_ld32(tmem + TM_S + 64u * slot + lane_off + 32, r1);
+                tmem_ld_wait64(r0, r1);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(tmem + TM_S + 64u * slot + lane_off + 32 * c, r);
-                    tmem_ld_wait32(r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
+                for (int i = 0; i < 32; ++i) {
+                    s[i] = __uint_as_float(r0[i]);
+                    s[32 + i] = __uint_as_float(r1[i]);
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(B_SEMPTY + slot));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_SEMPTY + slot));
             if (cur.last() && cur.p + 1 < cur.p_end) write_q(cur.p + 1);   // QK of this piece is complete
             // 2. add the peer's fp16 half
             if (leader) mbar_arrive_expect_tx(bar(B_XFULL + slot), X_BYTES);
@@ -426,37 +490,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     s[8 * c + 6] += f3.x; s[8 * c + 7] += f3.y;
                 }
             }
-            mbar_arrive_remote(peerfree_remote0 + 8u * slot);
-            // 3. online softmax in base 2 (both CTAs compute identical values)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_XREAD + slot));   // forwarded to the peer by a swap warp
+            // 3. online softmax in base 2; the maximum is taken on the raw
+            //    scores (the scale is positive) and the scale folded into the
+            //    exponent's FMA.  Columns past a row's visible length (only on
+            //    a unit's last tiles) are masked to -inf.
             const int32_t tok0 = cur.t * BN;
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (tok0 + BN > vis_lo) {
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                s[c] = (tok0 + c < vis) ? s[c] * a.scale_log2 : -INFINITY;
-                mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+                for (int c = 0; c < BN; ++c) s[c] = (tok0 + c < vis) ? s[c] : -INFINITY;
             }
-            const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+            for (int c = 4; c < BN; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+            const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
             float factor = 1.f;
             bool rescale = false;
             if (tmax > m_ref + kRescaleThreshold) {
                 if (m_ref != -INFINITY) {
-                    factor = exp2f(m_ref - tmax);
+                    factor = fast_exp2(m_ref - tmax);
                     rescale = true;
                 }
                 l *= factor;
                 m_ref = tmax;
             }
-            const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-            uint32_t pk[BN / 2];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < BN; c += 2) {
-                const float p0 = exp2f(s[c] - mref);        // exp2(-inf) = 0 for masked columns
-                const float p1 = exp2f(s[c + 1] - mref);
-                ls[(c >> 1) & 3] += p0 + p1;
-                pk[c / 2] = pack_bf16x2(p0, p1);
-            }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            const float neg_mref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            uint32_t pk[BN / 4];
+            l += (half == 0) ? exp_half<0>(s, a.scale_log2, neg_mref, pk) : exp_half<BN / 2>(s, a.scale_log2, neg_mref, pk);
             // 4. P slot reuse (PV of tile g-2) and O rescale (PV of tile g-1)
             ok = warp_wait(bar(B_PVDONE + slot), ph ^ 1u, abort_flag, status);
             if (!ok) break;
@@ -466,7 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float f = rescale ? factor : 1.f;
 #pragma unroll 1
-                for (int c0 = 0; c0 < 256; c0 += 32) {
+                for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tO + c0, r);
                     tmem_ld_wait32(r);
@@ -483,9 +544,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
             }
             // 5. last tile of a ragged unit: clear cache rows past the end so
-            //    that P = 0 never meets non-finite garbage in V
-            if (tok0 + BN > vis_max) {
-                const int32_t nvalid = max(0, vis_max - tok0);
+            //    that P = 0 never meets non-finite garbage in V (group 0 only)
+            if (half == 0 && tok0 + BN > vis_hi) {
+                const int32_t nvalid = max(0, vis_hi - tok0);
                 const int32_t nrows = BN - nvalid;
                 uint8_t* st_base = smem + OFF_KV + ((g % NSTAGE) * STAGE_BYTES);
                 const int32_t chunks = nrows * 8 * 4;
@@ -496,35 +557,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4*>(st_base + kb * KN_BLK + rr * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            // 6. P (bf16) -> smem, 128-byte swizzled K-major rows
+            // 6. this group's 32 columns of P (bf16) -> smem, 128-byte swizzled K-major rows
             {
                 uint8_t* prow = smem + OFF_P + slot * P_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(prow + ((c ^ rsw) * 16)) =
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(prow + (((4 * (int)half + c) ^ rsw) * 16)) =
                         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_PFULL + slot));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
             // 7. epilogue after the piece's last tile: O / l -> out or partial slot
             if (cur.last()) {
                 ok = warp_wait(bar(B_PVDONE + slot), ph, abort_flag, status);
                 if (!ok) break;
                 tc_fence_after();
-                const float inv_l = l > 0.f ? 1.f / l : 0.f;
-                const float row_lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+                // The row sum is split between the two groups: swap halves
+                // through shared memory.  Written only after the last PV of
+                // the piece, which needs the partner's P of that tile, so the
+                // partner has read the previous piece's value by now.
+                red[half * BM + row] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_LRED + quarter));
+                ok = warp_wait(bar(B_LRED + quarter), n_epi & 1u, abort_flag, status);
+                if (!ok) break;
+                ++n_epi;
+                const float l_tot = l + red[(half ^ 1u) * BM + row];
+                const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                const float row_lse = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
                 const bool store = row < rows_valid;
                 const int64_t grow = (int64_t)b * QH + qrow;
                 const int32_t slot_out = cur.pc.slot;
+                const int32_t col0 = 256 * (int32_t)rank + 128 * (int32_t)half;
 #pragma unroll 1
-                for (int c0 = 0; c0 < 256; c0 += 32) {
+                for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tO + c0, r);
                     tmem_ld_wait32(r);
                     if (store) {
                         if (slot_out < 0) {
                             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + grow * 512 +
-                                                                  256 * rank + c0);
+                                                                  col0 + c0);
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
                                 dst[q] = make_uint4(
@@ -534,7 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv_l, __uint_as_float(r[8 * q + 7]) * inv_l));
                         } else {
                             float4* dst = reinterpret_cast<float4*>(
-                                v.o_part + ((int64_t)slot_out * kRowsPerUnit + row) * 512 + 256 * rank + c0);
+                                v.o_part + ((int64_t)slot_out * kRowsPerUnit + row) * 512 + col0 + c0);
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
                                 dst[q] = make_float4(__uint_as_float(r[4 * q]) * inv_l,
@@ -544,7 +618,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (store && rank == 0) {
+                if (store && rank == 0 && half == 0) {
                     if (slot_out < 0) {
                         if (a.lse) a.lse[grow] = row_lse;
                     } else {
@@ -563,6 +637,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (quarter * 32u) << 16;
         const uint32_t x_remote0 = map_to_cta(sbase + OFF_X, peer);
         const uint32_t xfull_remote0 = map_to_cta(bar(B_XFULL), peer);
+        const uint32_t peerfree_remote0 = map_to_cta(bar(B_PEERFREE), peer);
+        const bool forwarder = (warp == 2 + kSoftmaxWarps) && lane == 0;
         const int rsw = row & 7;
         TileCursor cur;
         cur.init(v.pieces, p_begin, p_end);
@@ -575,18 +651,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             uint32_t h[BN / 2];
             {
-                uint32_t r[32];
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem + TM_S + 64u * slot + lane_off, r0);
+                tmem_ld32(tmem + TM_S + 64u * slot + lane_off + 32, r1);
+                tmem_ld_wait64(r0, r1);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(tmem + TM_S + 64u * slot + lane_off + 32 * c, r);
-                    tmem_ld_wait32(r);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        h[16 * c + i] = pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                for (int i = 0; i < 16; ++i) {
+                    h[i] = pack_f16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                    h[16 + i] = pack_f16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(B_SEMPTY + slot));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_SEMPTY + slot));
             ok = warp_wait<true>(bar(B_PEERFREE + slot), ph ^ 1u, abort_flag, status);
             if (!ok) break;
             const uint32_t dst = x_remote0 + slot * X_BYTES + (uint32_t)row * 128u;
@@ -594,6 +671,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 8; ++c)
                 st_async_v4(dst + (uint32_t)((c ^ rsw) * 16), h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3],
                             xfull_remote0 + 8u * slot);
+            // Forward "this CTA has read the peer's scores of tile g" to the
+            // peer (its swap warps may then refill that slot).  The remote
+            // arrive is slow, so it is kept off the softmax warps.
+            if (forwarder) {
+                ok = bounded_wait(bar(B_XREAD + slot), ph, abort_flag, status);
+                if (ok) mbar_arrive_remote(peerfree_remote0 + 8u * slot);
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
             ++g;
             cur.next();
         }

@@ -12,6 +12,7 @@ struct TcArgs {
     const int32_t* page_table;
     const int32_t* seq_lens;
     const void* q_nope;  // bf16 [B*Q*H][512]
+    const void* cache;   // bf16 [pages][64][576] (L2 prefetch addresses)
     void* out;          // bf16 [B*Q*H][512]
     float* lse;         // [B*Q*H] or null
     int32_t num_pages;
@@ -20,6 +21,7 @@ struct TcArgs {
     int32_t H;
     float scale_log2;   // softmax_scale * log2(e)
     int32_t evict_first;  // stream the cache with an evict-first L2 policy
+    int32_t prefetch_tiles;  // L2 prefetch distance of the cache stream, in tiles
     int64_t total_rows;   // B*Q*H
 };
 
@@ -32,6 +34,13 @@ struct TcMaps {
 // Dynamic shared memory of the kernel (bytes) and its cluster size.
 size_t decode_tc_smem_bytes();
 constexpr int kTcClusterSize = 2;
+// L2 prefetch distance of the cache stream (tiles ahead of the TMA loads of
+// a CTA; 0 = off).  Measured on the full-width workload it slowed the kernel
+// (the ring is not latency-starved), so it is off by default.
+#ifndef MLA_TC_PREFETCH_TILES
+#define MLA_TC_PREFETCH_TILES 0
+#endif
+constexpr int kTcPrefetchTiles = MLA_TC_PREFETCH_TILES;
 
 // Maximum number of co-resident 2-CTA clusters on the current device.
 cudaError_t decode_tc_max_clusters(int32_t* clusters);
