@@ -23,17 +23,17 @@
 // Each accumulates its 256 output columns O += P V with P (bf16) in smem and
 // the same cache tile read as an MN-major V operand.
 //
-// Pipeline (per CTA, 448 threads):
+// Pipeline (per CTA, 480 threads):
 //   warp 0      TMA producer: q_rope per piece, 4-stage ring of cache tiles
 //   warp 1      MMA issuer (owns TMEM); QK runs two tiles ahead of PV so the
 //               score swap of tile g+1 overlaps the softmax of tile g
-//   warps 2-9   softmax, two warpgroups on the same rows: each adds the
-//               peer's half, takes the row max over all 64 columns, and
-//               exponentiates / stores P for its own 32 columns; lazy O
-//               rescale and epilogue split by O columns; q_nope -> TMEM
-//   warps 10-13 score swap: S(g) from TMEM -> fp16 -> st.async to the peer;
-//               one thread forwards "scores read" to the peer (the remote
-//               arrive is slow, so it stays off the softmax warps)
+//   warps 2-9   softmax, two warpgroups taking alternate tiles (ping-pong):
+//               add the peer's half, online softmax with the running max
+//               handed between the groups, P -> smem, lazy O rescale,
+//               epilogue of a piece's last tile; q_nope -> TMEM
+//   warp 10     forwards "peer's scores read" to the peer (a slow remote
+//               arrive, kept off the softmax and swap warps)
+//   warps 11-14 score swap: S(g) from TMEM -> fp16 -> st.async to the peer
 // TMEM: O 256 columns | q_nope 128 | S double buffer 2 x 64.
 //
 // Every wait is bounded (ptx.cuh: bounded_wait); on a timeout the kernel
@@ -54,7 +54,8 @@ constexpr int BN = 64;           // tokens per tile (= page)
 constexpr int NSTAGE = 4;        // cache-tile ring depth
 constexpr int kSoftmaxWarps = 8;  // two warpgroups
 constexpr int kSwapWarps = 4;
-constexpr int kThreads = 32 * (2 + kSoftmaxWarps + kSwapWarps);   // 448
+constexpr int kForwardWarp = 2 + kSoftmaxWarps;                     // warp 10
+constexpr int kThreads = 32 * (3 + kSoftmaxWarps + kSwapWarps);   // 480
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_QR = 0;                               // 32 RoPE dims x 128 rows, 64B swizzle
@@ -68,8 +69,10 @@ constexpr uint32_t OFF_P = OFF_KV + NSTAGE * STAGE_BYTES;
 constexpr uint32_t X_BYTES = BM * BN * 2;                    // peer's fp16 partial scores
 constexpr uint32_t OFF_X = OFF_P + 2 * P_BYTES;
 constexpr uint32_t OFF_BAR = OFF_X + 2 * X_BYTES;
-constexpr uint32_t OFF_RED = OFF_BAR + 256;                   // [2 groups][128 rows] fp32 row sums
-constexpr uint32_t SMEM_USED = OFF_RED + 2 * BM * 4;
+constexpr uint32_t BAR_BYTES = 512;
+constexpr uint32_t OFF_M = OFF_BAR + BAR_BYTES;                // [2 slots][128 rows] fp32 running max
+constexpr uint32_t OFF_LM = OFF_M + 2 * BM * 4;                // [2][128] float2 (row sum, its max)
+constexpr uint32_t SMEM_USED = OFF_LM + 2 * BM * 8;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;            // + alignment slack
 
 static_assert(OFF_KV % 1024 == 0 && STAGE_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_X % 1024 == 0,
@@ -90,13 +93,16 @@ enum : int {
     B_PFULL = B_PEERFREE + 2,       // [2]
     B_PVDONE = B_PFULL + 2,         // [2]
     B_EXIT = B_PVDONE + 2,
-    B_LRED,                         // [4] row-sum swap of the two softmax warps sharing a lane quarter
-    B_XREAD = B_LRED + 4,           // [2] this CTA's softmax warps are done reading the peer's scores
-    NUM_BARS = B_XREAD + 2
+    B_XREAD,                        // [2] this CTA's softmax is done reading the peer's scores
+    B_MREADY = B_XREAD + 2,         // [2] running max after tile g published (slot g & 1)
+    B_LFULL = B_MREADY + 2,         // [2] a group's row sum of a piece published (piece parity)
+    B_LFREE = B_LFULL + 2,          // [2] ... and read
+    B_OFREE = B_LFREE + 2,          // epilogue has read O; the next piece may overwrite it
+    NUM_BARS
 };
-static_assert(NUM_BARS * 8 <= 240, "barrier area");
-constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 240;
-constexpr uint32_t OFF_ABORT = OFF_BAR + 244;
+static_assert(NUM_BARS * 8 <= BAR_BYTES - 16, "barrier area");
+constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + BAR_BYTES - 16;
+constexpr uint32_t OFF_ABORT = OFF_BAR + BAR_BYTES - 12;
 
 // TMEM columns
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384, TM_COLS = 512;
@@ -213,22 +219,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(B_QRFULL), 1);
         mbar_init(bar(B_QREMPTY), 1);
-        mbar_init(bar(B_QNFULL), kSoftmaxWarps);
+        mbar_init(bar(B_QNFULL), 4);
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(bar(B_KVFULL + s), 1);
             mbar_init(bar(B_KVEMPTY + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_SFULL + s), 1);
-            mbar_init(bar(B_SEMPTY + s), kSoftmaxWarps + kSwapWarps);
+            mbar_init(bar(B_SEMPTY + s), 4 + kSwapWarps);
             mbar_init(bar(B_XFULL + s), 1);
             mbar_init(bar(B_PEERFREE + s), 1);
-            mbar_init(bar(B_XREAD + s), kSoftmaxWarps);
-            mbar_init(bar(B_PFULL + s), kSoftmaxWarps);
+            mbar_init(bar(B_XREAD + s), 4);
+            mbar_init(bar(B_MREADY + s), 4);
+            mbar_init(bar(B_LFULL + s), 4);
+            mbar_init(bar(B_LFREE + s), 4);
+            mbar_init(bar(B_PFULL + s), 4);
             mbar_init(bar(B_PVDONE + s), 1);
         }
         mbar_init(bar(B_EXIT), 1);
-        for (int q = 0; q < 4; ++q) mbar_init(bar(B_LRED + q), 2);
+        mbar_init(bar(B_OFREE), 4);
         *abort_flag = 0;
         fence_mbar_init_cluster();
     }
@@ -320,7 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             TileCursor qk, pv;
             qk.init(v.pieces, p_begin, p_end);
             pv.init(v.pieces, p_begin, p_end);
-            uint32_t g_qk = 0, g_pv = 0, qk_stage = 0, qk_phase = 0, pv_stage = 0, q_cnt = 0;
+            uint32_t g_qk = 0, g_pv = 0, qk_stage = 0, qk_phase = 0, pv_stage = 0, q_cnt = 0, pv_piece = 0;
 
             auto issue_qk = [&]() -> bool {
                 const uint32_t slot = g_qk & 1u;
@@ -357,6 +366,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             };
             auto issue_pv = [&]() -> bool {
                 const uint32_t slot = g_pv & 1u;
+                if (pv.first() && pv_piece > 0) {
+                    if (!bounded_wait(bar(B_OFREE), (pv_piece - 1) & 1u, abort_flag, status)) return false;
+                }
+                if (pv.first()) ++pv_piece;
                 if (!bounded_wait(bar(B_PFULL + slot), (g_pv >> 1) & 1u, abort_flag, status)) return false;
                 tc_fence_after();
                 const uint32_t sk = sbase + OFF_KV + pv_stage * STAGE_BYTES;
@@ -388,34 +401,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 2 + kSoftmaxWarps) {
         // ------------------------------------- softmax / correction / epilogue
-        // Two warpgroups; both hold the same 128 rows (one thread per row and
-        // group).  Each computes the row maximum over all 64 columns of the
-        // tile (so both take identical rescale decisions without talking to
-        // each other), but exponentiates only its own half of the columns,
-        // rescales and stores only its own half of the 256 O columns.
-        const uint32_t half = (uint32_t)((warp - 2) >> 2);
+        // Two warpgroups take alternate tiles (group g & 1 owns tile g), so
+        // the long latency chain of one tile's softmax overlaps the next
+        // tile's.  Within a group one thread owns one row.  The running
+        // maximum is handed from the owner of tile g-1 to the owner of tile g
+        // through shared memory (B_MREADY); each group keeps the row sum of
+        // its own tiles relative to the latest maximum it has seen, and the
+        // two sums are merged at the end of a piece (B_LFULL / B_LFREE).  The
+        // owner of a piece's last tile writes the epilogue and then releases
+        // O to the MMA warp (B_OFREE).
+        const uint32_t wg = (uint32_t)((warp - 2) >> 2);
         const uint32_t quarter = (uint32_t)(warp & 3);
         const int32_t row = (int32_t)(quarter * 32 + lane);
         const uint32_t lane_off = (quarter * 32u) << 16;
-        const uint32_t tO = tmem + TM_O + lane_off + 128u * half;
-        const uint32_t tQ = tmem + TM_Q + lane_off + 64u * half;
-        const bool leader = (threadIdx.x == 64);
+        const uint32_t tO = tmem + TM_O + lane_off, tQ = tmem + TM_Q + lane_off;
+        const bool leader = (warp == 2 + 4 * (int)wg) && lane == 0;
+        const int32_t gtid = (int32_t)threadIdx.x - 64 - 128 * (int32_t)wg;   // 0..127 within the group
         const int rsw = row & 7;
-        float* red = reinterpret_cast<float*>(smem + OFF_RED);
+        float* mrow = reinterpret_cast<float*>(smem + OFF_M);     // [2 slots][128 rows] running max
+        float2* lm = reinterpret_cast<float2*>(smem + OFF_LM);    // [2][128] (row sum, its max) of a group
         bool ok = true;
 
-        // this group's half of q_nope (128 of the rank's 256 dims) for piece
-        // `pp` -> TMEM (A operand of QK)
+        // q_nope columns of this rank for piece `pp` -> TMEM (A operand of QK)
         auto write_q = [&](int32_t pp) {
             const Piece pc = v.pieces[pp];
-            const int32_t b = pc.unit / RB, rb = pc.unit % RB;
-            const int32_t rows_valid = min(BM, QH - rb * BM);
-            const int64_t grow = (int64_t)b * QH + rb * BM + row;
+            const int32_t qb = pc.unit / RB, qrb = pc.unit % RB;
+            const int32_t qrows = min(BM, QH - qrb * BM);
+            const int64_t grow = (int64_t)qb * QH + qrb * BM + row;
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_nope) +
-                                                              grow * 512 + 256 * rank + 128 * half);
-            const bool have = row < rows_valid;
+                                                              grow * 512 + 256 * rank);
+            const bool have = row < qrows;
 #pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 32) {
+            for (int c0 = 0; c0 < 128; c0 += 32) {
                 uint32_t r0[16], r1[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -435,12 +452,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
         TileCursor cur;
         cur.init(v.pieces, p_begin, p_end);
-        if (cur.valid()) write_q(cur.p);
-        uint32_t g = 0, n_epi = 0;
+        if (wg == 0 && cur.valid()) write_q(cur.p);
+        uint32_t g = 0, k = 0;   // tile and piece counters of this worker
         int32_t b = 0, rb = 0, rows_valid = 0, vis = 0, vis_lo = 0, vis_hi = 0, qrow = 0;
-        float m_ref = -INFINITY, l = 0.f;
-        while (ok && cur.valid()) {
-            const uint32_t slot = g & 1u, ph = (g >> 1) & 1u;
+        float m_seen = -INFINITY, l = 0.f;
+        for (; ok && cur.valid(); ++g, cur.next()) {
             if (cur.first()) {
                 b = cur.pc.unit / RB;
                 rb = cur.pc.unit % RB;
@@ -450,9 +466,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 vis = row < rows_valid ? visible_len(len, a.Q, a.H, qrow) : 0;
                 vis_lo = visible_len(len, a.Q, a.H, rb * BM);                    // fewest keys of the unit
                 vis_hi = visible_len(len, a.Q, a.H, rb * BM + rows_valid - 1);   // most keys of the unit
-                m_ref = -INFINITY;
+                m_seen = -INFINITY;
                 l = 0.f;
             }
+            if ((g & 1u) != wg) {
+                // not ours; after a piece's last tile publish this group's row sum
+                if (cur.last()) {
+                    ok = warp_wait(bar(B_LFREE + (k & 1u)), ((k >> 1) & 1u) ^ 1u, abort_flag, status);
+                    if (!ok) break;
+                    lm[(k & 1u) * BM + row] = make_float2(l, m_seen);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_LFULL + (k & 1u)));
+                    ++k;
+                }
+                continue;
+            }
+            const uint32_t slot = wg, ph = (g >> 1) & 1u;
             // 1. own partial S of tile g (all 64 columns)
             ok = warp_wait(bar(B_SFULL + slot), ph, abort_flag, status);
             if (!ok) break;
@@ -491,11 +520,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_XREAD + slot));   // forwarded to the peer by a swap warp
-            // 3. online softmax in base 2; the maximum is taken on the raw
-            //    scores (the scale is positive) and the scale folded into the
-            //    exponent's FMA.  Columns past a row's visible length (only on
-            //    a unit's last tiles) are masked to -inf.
+            if (lane == 0) mbar_arrive(bar(B_XREAD + slot));   // forwarded to the peer by warp kForwardWarp
+            // 3. tile maximum on the raw scores (the scale is positive);
+            //    columns past a row's visible length are masked to -inf
             const int32_t tok0 = cur.t * BN;
             if (tok0 + BN > vis_lo) {
 #pragma unroll
@@ -505,29 +532,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 4; c < BN; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
             const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
-            float factor = 1.f;
+            // 4. running maximum after tile g-1 (the other group's), lazy
+            //    update: O is rescaled only when the max grows by > 2^8
+            float m_prev = -INFINITY;
+            if (g > 0) {
+                ok = warp_wait(bar(B_MREADY + (slot ^ 1u)), ((g - 1) >> 1) & 1u, abort_flag, status);
+                if (!ok) break;
+                if (!cur.first()) m_prev = mrow[(slot ^ 1u) * BM + row];
+            }
+            float m_cur = m_prev, factor = 1.f;
             bool rescale = false;
-            if (tmax > m_ref + kRescaleThreshold) {
-                if (m_ref != -INFINITY) {
-                    factor = fast_exp2(m_ref - tmax);
+            if (tmax > m_prev + kRescaleThreshold) {
+                if (m_prev != -INFINITY) {
+                    factor = fast_exp2(m_prev - tmax);
                     rescale = true;
                 }
-                l *= factor;
-                m_ref = tmax;
+                m_cur = tmax;
             }
-            const float neg_mref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            uint32_t pk[BN / 4];
-            l += (half == 0) ? exp_half<0>(s, a.scale_log2, neg_mref, pk) : exp_half<BN / 2>(s, a.scale_log2, neg_mref, pk);
-            // 4. P slot reuse (PV of tile g-2) and O rescale (PV of tile g-1)
+            mrow[slot * BM + row] = m_cur;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_MREADY + slot));
+            if (m_seen != -INFINITY && m_cur != m_seen) l *= fast_exp2(m_seen - m_cur);
+            m_seen = m_cur;
+            // 5. P slot free (PV of tile g-2), then P = 2^(x - m) as bf16,
+            //    128-byte swizzled K-major rows, 8 columns at a time
             ok = warp_wait(bar(B_PVDONE + slot), ph ^ 1u, abort_flag, status);
             if (!ok) break;
+            {
+                const float neg_m = (m_cur == -INFINITY) ? 0.f : -m_cur;
+                uint8_t* prow = smem + OFF_P + slot * P_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float p0 = fast_exp2(fmaf(s[8 * c + 2 * i], a.scale_log2, neg_m));   // exp2(-inf) = 0
+                        const float p1 = fast_exp2(fmaf(s[8 * c + 2 * i + 1], a.scale_log2, neg_m));
+                        ls[i] += p0 + p1;
+                        w[i] = pack_bf16x2(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(prow + ((c ^ rsw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            }
+            // 6. O rescale (after the PV of tile g-1, before the PV of tile g)
             if (__any_sync(0xffffffffu, rescale)) {
                 ok = warp_wait(bar(B_PVDONE + (slot ^ 1u)), ((g - 1) >> 1) & 1u, abort_flag, status);
                 if (!ok) break;
                 tc_fence_after();
                 const float f = rescale ? factor : 1.f;
 #pragma unroll 1
-                for (int c0 = 0; c0 < 128; c0 += 32) {
+                for (int c0 = 0; c0 < 256; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tO + c0, r);
                     tmem_ld_wait32(r);
@@ -543,55 +599,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
             }
-            // 5. last tile of a ragged unit: clear cache rows past the end so
-            //    that P = 0 never meets non-finite garbage in V (group 0 only)
-            if (half == 0 && tok0 + BN > vis_hi) {
+            // 7. last tile of a ragged unit: clear cache rows past the end so
+            //    that P = 0 never meets non-finite garbage in V
+            if (tok0 + BN > vis_hi) {
                 const int32_t nvalid = max(0, vis_hi - tok0);
                 const int32_t nrows = BN - nvalid;
                 uint8_t* st_base = smem + OFF_KV + ((g % NSTAGE) * STAGE_BYTES);
                 const int32_t chunks = nrows * 8 * 4;
-                for (int32_t i = (int32_t)threadIdx.x - 64; i < chunks; i += 128) {
+                for (int32_t i = gtid; i < chunks; i += 128) {
                     const int32_t kb = i / (nrows * 8);
                     const int32_t rem = i % (nrows * 8);
                     const int32_t rr = nvalid + rem / 8, cc = rem % 8;
                     *reinterpret_cast<uint4*>(st_base + kb * KN_BLK + rr * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            // 6. this group's 32 columns of P (bf16) -> smem, 128-byte swizzled K-major rows
-            {
-                uint8_t* prow = smem + OFF_P + slot * P_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4*>(prow + (((4 * (int)half + c) ^ rsw) * 16)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            }
+            // 8. publish P(g)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PFULL + slot));
-            // 7. epilogue after the piece's last tile: O / l -> out or partial slot
+            // 9. epilogue after the piece's last tile: O / l -> out or partial slot
             if (cur.last()) {
                 ok = warp_wait(bar(B_PVDONE + slot), ph, abort_flag, status);
                 if (!ok) break;
-                tc_fence_after();
-                // The row sum is split between the two groups: swap halves
-                // through shared memory.  Written only after the last PV of
-                // the piece, which needs the partner's P of that tile, so the
-                // partner has read the previous piece's value by now.
-                red[half * BM + row] = l;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_LRED + quarter));
-                ok = warp_wait(bar(B_LRED + quarter), n_epi & 1u, abort_flag, status);
+                ok = warp_wait(bar(B_LFULL + (k & 1u)), (k >> 1) & 1u, abort_flag, status);
                 if (!ok) break;
-                ++n_epi;
-                const float l_tot = l + red[(half ^ 1u) * BM + row];
+                const float2 other = lm[(k & 1u) * BM + row];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_LFREE + (k & 1u)));
+                ++k;
+                tc_fence_after();
+                // the other group's sum is relative to the max it last saw (<= m_seen)
+                const float l_tot = l + (other.y == -INFINITY ? 0.f : other.x * fast_exp2(other.y - m_seen));
                 const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-                const float row_lse = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
+                const float row_lse = l_tot > 0.f ? (m_seen + log2f(l_tot)) * kLn2 : -INFINITY;
                 const bool store = row < rows_valid;
                 const int64_t grow = (int64_t)b * QH + qrow;
                 const int32_t slot_out = cur.pc.slot;
-                const int32_t col0 = 256 * (int32_t)rank + 128 * (int32_t)half;
+                const int32_t col0 = 256 * (int32_t)rank;
 #pragma unroll 1
-                for (int c0 = 0; c0 < 128; c0 += 32) {
+                for (int c0 = 0; c0 < 256; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tO + c0, r);
                     tmem_ld_wait32(r);
@@ -618,7 +664,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (store && rank == 0 && half == 0) {
+                if (store && rank == 0) {
                     if (slot_out < 0) {
                         if (a.lse) a.lse[grow] = row_lse;
                     } else {
@@ -626,9 +672,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_OFREE));   // O may be overwritten by the next piece
             }
-            ++g;
-            cur.next();
+        }
+    } else if (warp == kForwardWarp) {
+        // ------------------------------------------- "scores read" forwarder
+        // Tells the peer that this CTA's softmax warps have read the scores
+        // it sent for tile g, so its swap warps may refill that slot.  A
+        // cluster-scope remote arrive takes ~1,000 cycles, so it gets a warp
+        // of its own instead of sitting on the softmax or swap critical path.
+        if (lane == 0) {
+            const uint32_t peerfree_remote0 = map_to_cta(bar(B_PEERFREE), peer);
+            TileCursor cur;
+            cur.init(v.pieces, p_begin, p_end);
+            for (uint32_t g = 0; cur.valid(); ++g, cur.next()) {
+                if (!bounded_wait(bar(B_XREAD + (g & 1u)), (g >> 1) & 1u, abort_flag, status)) break;
+                mbar_arrive_remote(peerfree_remote0 + 8u * (g & 1u));
+            }
         }
     } else {
         // ------------------------------------------------ score swap (fp16)
@@ -637,8 +698,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (quarter * 32u) << 16;
         const uint32_t x_remote0 = map_to_cta(sbase + OFF_X, peer);
         const uint32_t xfull_remote0 = map_to_cta(bar(B_XFULL), peer);
-        const uint32_t peerfree_remote0 = map_to_cta(bar(B_PEERFREE), peer);
-        const bool forwarder = (warp == 2 + kSoftmaxWarps) && lane == 0;
         const int rsw = row & 7;
         TileCursor cur;
         cur.init(v.pieces, p_begin, p_end);
@@ -671,14 +730,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 8; ++c)
                 st_async_v4(dst + (uint32_t)((c ^ rsw) * 16), h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3],
                             xfull_remote0 + 8u * slot);
-            // Forward "this CTA has read the peer's scores of tile g" to the
-            // peer (its swap warps may then refill that slot).  The remote
-            // arrive is slow, so it is kept off the softmax warps.
-            if (forwarder) {
-                ok = bounded_wait(bar(B_XREAD + slot), ph, abort_flag, status);
-                if (ok) mbar_arrive_remote(peerfree_remote0 + 8u * slot);
-            }
-            if (!__all_sync(0xffffffffu, ok)) break;
             ++g;
             cur.next();
         }
