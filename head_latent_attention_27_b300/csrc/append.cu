@@ -6,9 +6,13 @@
 // page, section 2(3).)
 //
 // One warp per token.  The latent part is fp32 arithmetic with one rounding
-// to the cache dtype; the RoPE angle pos * base^(-2i/d_r) and its sine and
-// cosine are computed in fp64 so that large positions keep full accuracy.
+// to the cache dtype.  The RoPE frequencies are computed once on the host in
+// fp64; per pair the angle pos * theta_i is formed and reduced modulo 2 pi in
+// fp64 (three operations), and sine and cosine are taken in fp32 of the
+// reduced angle, so large positions keep full accuracy without fp64
+// transcendental functions (slow on this GPU).
 #include <cuda_bf16.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "append.cuh"
@@ -70,10 +74,11 @@ __global__ void __launch_bounds__(kWarps * 32)
         const float x0 = load_f(kx + 2 * i), x1 = load_f(kx + 2 * i + 1);
         float y0 = x0, y1 = x1;
         if (a.flags & 2u) {
-            const double theta = pow((double)a.rope_base, -2.0 * (double)i / (double)a.d_r);
-            double s, c;
-            sincos((double)pos * theta, &s, &c);
-            const float cf = (float)c, sf = (float)s;
+            constexpr double kTwoPi = 6.283185307179586476925286766559;
+            const double ang = (double)pos * a.theta[i];
+            const double r = fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);   // in [-pi, pi]
+            float sf, cf;
+            sincosf((float)r, &sf, &cf);
             y0 = x0 * cf - x1 * sf;
             y1 = x0 * sf + x1 * cf;
         }
@@ -84,9 +89,12 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 }  // namespace
 
-cudaError_t launch_append(const AppendArgs& a, const void* ckv, const void* kr, int32_t in_dtype,
+cudaError_t launch_append(const AppendArgs& args, const void* ckv, const void* kr, int32_t in_dtype,
                           int32_t cache_dtype, void* cache, cudaStream_t stream) {
-    if (a.T == 0) return cudaSuccess;
+    if (args.T == 0) return cudaSuccess;
+    AppendArgs a = args;
+    for (int32_t i = 0; i < 32; ++i)
+        a.theta[i] = (i < a.d_r / 2) ? pow((double)a.rope_base, -2.0 * (double)i / (double)a.d_r) : 0.0;
     const dim3 grid((a.T + kWarps - 1) / kWarps);
     const dim3 block(kWarps * 32);
     if (in_dtype == 0 && cache_dtype == 0)

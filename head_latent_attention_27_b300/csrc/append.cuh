@@ -20,6 +20,9 @@ struct AppendArgs {
     uint32_t flags;
     float eps;
     float rope_base;
+    // RoPE frequencies theta_i = rope_base^(-2i/d_r), i < d_r/2, in fp64
+    // (filled by launch_append on the host).
+    double theta[32];
 };
 
 cudaError_t launch_append(const AppendArgs& a, const void* ckv, const void* kr, int32_t in_dtype,

@@ -30,33 +30,56 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     if (n == 1) return;
     const int64_t grow = (int64_t)b * QH + (int64_t)rb * kRowsPerUnit + row;
 
+    const float* lp = v.lse_part + (int64_t)p0 * kRowsPerUnit + row;   // lse of piece k: lp[k * 128]
     float m = -INFINITY;
-    for (int32_t k = 0; k < n; ++k) m = fmaxf(m, v.lse_part[(int64_t)(p0 + k) * kRowsPerUnit + row]);
+    for (int32_t k = 0; k < n; ++k) m = fmaxf(m, lp[(int64_t)k * kRowsPerUnit]);
     float total_lse = -INFINITY;
-    float z = 0.f;
     if (m != -INFINITY) {
-        for (int32_t k = 0; k < n; ++k) z += expf(v.lse_part[(int64_t)(p0 + k) * kRowsPerUnit + row] - m);
+        float z = 0.f;
+        for (int32_t k = 0; k < n; ++k) z += expf(lp[(int64_t)k * kRowsPerUnit] - m);
         total_lse = m + logf(z);
     }
-    // out = sum_k w_k o_k with w_k = exp(lse_k - lse)
+    // out = sum_k w_k o_k with w_k = exp(lse_k - lse); the weights of the
+    // first kCached pieces are computed once per row
+    constexpr int kCached = 8;
+    float wc[kCached];
+#pragma unroll
+    for (int k = 0; k < kCached; ++k) {
+        const float lk = k < n ? lp[(int64_t)k * kRowsPerUnit] : -INFINITY;
+        wc[k] = (total_lse != -INFINITY && lk != -INFINITY) ? expf(lk - total_lse) : 0.f;
+    }
+    const float* ob = v.o_part + ((int64_t)p0 * kRowsPerUnit + row) * d_c;   // piece k: ob + k * 128 * d_c
+    const int64_t pstride = (int64_t)kRowsPerUnit * d_c;
     for (int32_t c0 = lane * 4; c0 < d_c; c0 += 128) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (total_lse != -INFINITY) {
-            for (int32_t k = 0; k < n; ++k) {
-                const float lk = v.lse_part[(int64_t)(p0 + k) * kRowsPerUnit + row];
-                if (lk == -INFINITY) continue;
-                const float w = expf(lk - total_lse);
-                const float* src = v.o_part + ((int64_t)(p0 + k) * kRowsPerUnit + row) * d_c + c0;
-                if (c0 + 4 <= d_c) {
-                    const float4 o = *reinterpret_cast<const float4*>(src);
-                    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-                } else {
-                    const int32_t rem = d_c - c0;
-                    acc.x += w * src[0];
-                    if (rem > 1) acc.y += w * src[1];
-                    if (rem > 2) acc.z += w * src[2];
-                }
+        const bool full = c0 + 4 <= d_c;
+        for (int32_t k = 0; k < n; ++k) {
+            float w;
+            if (k < kCached) {
+                w = wc[k];
+            } else {
+                const float lk = lp[(int64_t)k * kRowsPerUnit];
+                w = (total_lse != -INFINITY && lk != -INFINITY) ? expf(lk - total_lse) : 0.f;
             }
+            if (w == 0.f) continue;
+            const float* src = ob + k * pstride + c0;
+            if (full) {
+                const float4 o = *reinterpret_cast<const float4*>(src);
+                acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+            } else {
+                const int32_t rem = d_c - c0;
+                acc.x += w * src[0];
+                if (rem > 1) acc.y += w * src[1];
+                if (rem > 2) acc.z += w * src[2];
+            }
+        }
+        if (out_bf16 && full) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + grow * d_c + c0) = pk;
+            continue;
         }
         const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
         const int32_t cnt = min(4, d_c - c0);
