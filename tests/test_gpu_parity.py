@@ -119,6 +119,28 @@ def test_bf16_three_phases_equal_one_call():
     compare(w, out1, lse1)
 
 
+def test_bf16_one_plan_serves_several_attention_launches():
+    """A caller decoding several layers with the same lengths plans once and
+    runs the attention kernel per layer; split units must merge every time."""
+    mla = mla_pkg()
+    w = synth.custom_bf16("plan_reuse", 705, [4096, 4096, 700, 64, 3001], H=128, Q=1, paged=True)
+    cache, d = build_cache(w)
+    scale = 1.0 / math.sqrt(w.d_h + w.d_r)
+    ws = mla.alloc_workspace(w.B, w.Q, w.H, w.d_c, 0, "cuda")
+    mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws)
+    outs = []
+    for _ in range(3):
+        out = torch.full((w.B, w.Q, w.H, w.d_c), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((w.B, w.Q, w.H), float("nan"), dtype=torch.float32, device="cuda")
+        mla.mla_decode_attend(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, ws, lse=lse, softmax_scale=scale)
+        mla.mla_decode_combine(cache, out, ws, lse=lse)
+        assert mla.mla_decode_read_status(ws) == mla.MLA_OK
+        outs.append((out.double().cpu().numpy(), lse.double().cpu().numpy()))
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+    compare(w, *outs[0])
+
+
 def test_bf16_many_short_sequences_more_units_than_workers():
     lens = synth.uniform_int(703, 5, 300, 1, 300)
     w = synth.custom_bf16("many_short", 703, lens, H=128, Q=1, paged=True)
