@@ -11,6 +11,7 @@ figure through host buffers and the fp64 oracle's CPU throughput are
 reported alongside.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --profile-attend N   # build, plan once, N attention launches, no timing (for ncu)
 """
 from __future__ import annotations
 
@@ -414,17 +415,49 @@ def run_cuda(args, w):
         dist.destroy_process_group()
 
 
+def run_profile_attend(w, n: int) -> None:
+    """The attention kernel alone, `n` launches on one plan, for profilers."""
+    import torch
+
+    import head_latent_attention_27_b300 as mla
+    from synth.device import empty_pool, upload
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    d = upload(w, dev)
+    pool = empty_pool(w, dev, fill_nan=False)
+    cache = mla.Cache(pool, d["page_table"], w.d_c, w.d_r)
+    mla.mla_cache_append(cache, d["raw_c"], d["raw_k"], d["seq_ids"], d["positions"], eps=w.eps,
+                         rope_base=w.rope_base, flags=mla.MLA_APPEND_RMSNORM | mla.MLA_APPEND_ROPE)
+    out = torch.empty((w.B, w.Q, w.H, w.d_c), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Q, w.H), dtype=torch.float32, device=dev)
+    ws = mla.alloc_workspace(w.B, w.Q, w.H, w.d_c, 0, dev)
+    mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws)
+    for _ in range(n):
+        mla.mla_decode_attend(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, ws, lse=lse,
+                              softmax_scale=1.0 / math.sqrt(w.d_h + w.d_r))
+    torch.cuda.synchronize(dev)
+    status = mla.mla_decode_read_status(ws)
+    if status != mla.MLA_OK:
+        raise RuntimeError(f"kernel status {mla.mla_status_string(status)}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--profile-attend", type=int, default=0, metavar="N",
+                    help="run N attention launches on one plan and exit (no timing; for ncu)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "cuda":
         args.warmup = 3
     import synth
     w = synth.full_width()
+    if args.profile_attend > 0:
+        run_profile_attend(w, args.profile_attend)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

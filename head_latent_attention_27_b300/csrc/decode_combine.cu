@@ -50,45 +50,46 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     }
     const float* ob = v.o_part + ((int64_t)p0 * kRowsPerUnit + row) * d_c;   // piece k: ob + k * 128 * d_c
     const int64_t pstride = (int64_t)kRowsPerUnit * d_c;
-    for (int32_t c0 = lane * 4; c0 < d_c; c0 += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const bool full = c0 + 4 <= d_c;
-        for (int32_t k = 0; k < n; ++k) {
-            float w;
-            if (k < kCached) {
-                w = wc[k];
-            } else {
-                const float lk = lp[(int64_t)k * kRowsPerUnit];
-                w = (total_lse != -INFINITY && lk != -INFINITY) ? expf(lk - total_lse) : 0.f;
-            }
-            if (w == 0.f) continue;
-            const float* src = ob + k * pstride + c0;
-            if (full) {
-                const float4 o = *reinterpret_cast<const float4*>(src);
-                acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-            } else {
-                const int32_t rem = d_c - c0;
-                acc.x += w * src[0];
-                if (rem > 1) acc.y += w * src[1];
-                if (rem > 2) acc.z += w * src[2];
-            }
+    // each lane owns up to 4 chunks of 4 columns (d_c <= 512, a multiple of
+    // 4); all of a piece's loads are issued before they are used
+    constexpr int kChunks = 4;
+    float4 acc[kChunks];
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int32_t k = 0; k < n; ++k) {
+        float w;
+        if (k < kCached) {
+            w = wc[k];
+        } else {
+            const float lk = lp[(int64_t)k * kRowsPerUnit];
+            w = (total_lse != -INFINITY && lk != -INFINITY) ? expf(lk - total_lse) : 0.f;
         }
-        if (out_bf16 && full) {
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        if (w == 0.f) continue;
+        float4 x[kChunks];
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+            const int32_t c0 = lane * 4 + 128 * j;
+            x[j] = c0 < d_c ? *reinterpret_cast<const float4*>(ob + k * pstride + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+            acc[j].x += w * x[j].x; acc[j].y += w * x[j].y; acc[j].z += w * x[j].z; acc[j].w += w * x[j].w;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        const int32_t c0 = lane * 4 + 128 * j;
+        if (c0 >= d_c) continue;
+        if (out_bf16) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x, acc[j].y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z, acc[j].w);
             uint2 pk;
             pk.x = *reinterpret_cast<const uint32_t*>(&lo);
             pk.y = *reinterpret_cast<const uint32_t*>(&hi);
             *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + grow * d_c + c0) = pk;
-            continue;
-        }
-        const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
-        const int32_t cnt = min(4, d_c - c0);
-        if (out_bf16) {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + grow * d_c + c0;
-            for (int32_t i = 0; i < cnt; ++i) dst[i] = __float2bfloat16_rn(vals[i]);
-        } else {
+        } else {   // fp32 output is only guaranteed 4-byte alignment
             float* dst = static_cast<float*>(out) + grow * d_c + c0;
-            for (int32_t i = 0; i < cnt; ++i) dst[i] = vals[i];
+            dst[0] = acc[j].x; dst[1] = acc[j].y; dst[2] = acc[j].z; dst[3] = acc[j].w;
         }
     }
     if (lse != nullptr && lane == 0) lse[grow] = total_lse;
