@@ -43,11 +43,25 @@ class mla_cache_t(ctypes.Structure):
     ]
 
 
+class mla_rope_t(ctypes.Structure):
+    """RoPE parameters; yarn_factor > 1 applies YaRN's frequency interpolation."""
+    _fields_ = [
+        ("base", ctypes.c_float),
+        ("yarn_factor", ctypes.c_float),
+        ("yarn_alpha", ctypes.c_float),
+        ("yarn_beta", ctypes.c_float),
+        ("original_max_position", ctypes.c_int32),
+    ]
+
+
 _vp, _i32, _u32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t
 _pc = ctypes.POINTER(mla_cache_t)
 
 _SIGS = {
     "mla_cache_append": (_i32, [_pc, _vp, _vp, _i32, _vp, _f32, _f32, _vp, _vp, _i32, _u32, _vp]),
+    "mla_cache_append_rope": (_i32, [_pc, _vp, _vp, _i32, _vp, _f32, ctypes.POINTER(mla_rope_t), _vp, _vp, _i32, _u32,
+                                     _vp]),
+    "mla_yarn_softmax_scale": (_f32, [_f32, _f32, _f32]),
     "mla_decode": (_i32, [_pc, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
     "mla_decode_split_combine": (_i32, [_pc, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "mla_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
@@ -156,6 +170,38 @@ def mla_cache_append(cache: Cache, ckv_raw, kr_raw, seq_ids, positions, gamma=No
     _check(_lib.mla_cache_append(ctypes.byref(cc), _ptr(ckv_raw), _ptr(kr_raw), _dtype_code(ckv_raw), _ptr(gamma),
                                  float(eps), float(rope_base), _ptr(seq_ids), _ptr(positions), T, int(flags),
                                  _stream(stream)), "mla_cache_append")
+
+
+def mla_cache_append_rope(cache: Cache, ckv_raw, kr_raw, seq_ids, positions, rope: "mla_rope_t", gamma=None,
+                          eps: float = 1e-6, flags: int = MLA_APPEND_RMSNORM | MLA_APPEND_ROPE, stream=None) -> None:
+    """mla_cache_append with explicit RoPE parameters (YaRN when rope.yarn_factor > 1)."""
+    torch = _torch()
+    _need(ckv_raw, "ckv_raw", ndim=2)
+    _need(kr_raw, "kr_raw", ckv_raw.dtype, 2)
+    _need(seq_ids, "seq_ids", torch.int32, 1)
+    _need(positions, "positions", torch.int32, 1)
+    T = ckv_raw.shape[0]
+    if kr_raw.shape[0] != T or seq_ids.shape[0] != T or positions.shape[0] != T:
+        raise ValueError("row counts differ")
+    if ckv_raw.shape[1] != cache.d_c or kr_raw.shape[1] != cache.d_r:
+        raise ValueError("row widths do not match the cache")
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, 1)
+    cc = cache.c()
+    _check(_lib.mla_cache_append_rope(ctypes.byref(cc), _ptr(ckv_raw), _ptr(kr_raw), _dtype_code(ckv_raw),
+                                      _ptr(gamma), float(eps), ctypes.byref(rope), _ptr(seq_ids), _ptr(positions), T,
+                                      int(flags), _stream(stream)), "mla_cache_append_rope")
+
+
+def yarn_rope(base: float = 10000.0, factor: float = 40.0, alpha: float = 1.0, beta: float = 32.0,
+              original_max_position: int = 4096) -> "mla_rope_t":
+    """RoPE parameters of a YaRN-extended context (defaults: DeepSeek-V2's s=40, alpha=1, beta=32, 4K window)."""
+    return mla_rope_t(base, factor, alpha, beta, original_max_position)
+
+
+def mla_yarn_softmax_scale(softmax_scale: float, yarn_factor: float, coef: float = 0.0707) -> float:
+    """softmax_scale * (coef * ln(s) + 1)^2: YaRN's attention temperature on the softmax scale."""
+    return float(_lib.mla_yarn_softmax_scale(float(softmax_scale), float(yarn_factor), float(coef)))
 
 
 def mla_decode_workspace_size(B: int, Q: int, H: int, d_c: int = 512, n_split: int = 0, num_sms: int = 0) -> int:

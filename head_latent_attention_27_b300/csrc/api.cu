@@ -224,6 +224,31 @@ mla_status_t run_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeSha
     return do_combine(c, s, out, lse, ws, ws_bytes, stream);
 }
 
+// RoPE frequencies of the d_r/2 pairs in fp64 (plain RoPE, or YaRN's
+// piecewise interpolation when yarn_factor > 1); false for invalid params.
+bool rope_frequencies(const mla_rope_t& r, int32_t d_r, double theta[32]) {
+    if (!(r.base > 0.f) || !(r.yarn_factor >= 1.f) || !(r.yarn_beta > r.yarn_alpha) || r.original_max_position < 1 ||
+        d_r > 64)
+        return false;
+    const double kTwoPi = 6.283185307179586476925286766559;
+    for (int32_t i = 0; i < 32; ++i) {
+        if (i >= d_r / 2) {
+            theta[i] = 0.0;
+            continue;
+        }
+        const double t = pow((double)r.base, -2.0 * (double)i / (double)d_r);
+        if (r.yarn_factor == 1.f) {
+            theta[i] = t;
+            continue;
+        }
+        const double turns = (double)r.original_max_position * t / kTwoPi;
+        double g = (turns - (double)r.yarn_alpha) / ((double)r.yarn_beta - (double)r.yarn_alpha);
+        g = g < 0.0 ? 0.0 : (g > 1.0 ? 1.0 : g);
+        theta[i] = t * (g + (1.0 - g) / (double)r.yarn_factor);
+    }
+    return true;
+}
+
 // ------------------------------------------------- bounded-wait self-test --
 
 __global__ void selftest_wait_kernel(int* status, uint32_t timeout_us) {
@@ -257,9 +282,10 @@ using namespace mla;
 
 extern "C" {
 
-mla_status_t mla_cache_append(const mla_cache_t* cache, const void* ckv_raw, const void* kr_raw, int32_t in_dtype,
-                              const float* gamma, float eps, float rope_base, const int32_t* seq_ids,
-                              const int32_t* positions, int32_t T, uint32_t flags, void* stream) {
+mla_status_t mla_cache_append_rope(const mla_cache_t* cache, const void* ckv_raw, const void* kr_raw,
+                                   int32_t in_dtype, const float* gamma, float eps, const mla_rope_t* rope,
+                                   const int32_t* seq_ids, const int32_t* positions, int32_t T, uint32_t flags,
+                                   void* stream) {
     mla_status_t st = check_cache(cache);
     if (st != MLA_OK) return st;
     if (T < 0 || (in_dtype != MLA_BF16 && in_dtype != MLA_FP32)) return MLA_ERR_INVALID_ARG;
@@ -267,8 +293,12 @@ mla_status_t mla_cache_append(const mla_cache_t* cache, const void* ckv_raw, con
     if (T == 0) return MLA_OK;
     if (!ckv_raw || (cache->d_r > 0 && !kr_raw) || !seq_ids || !positions) return MLA_ERR_INVALID_ARG;
     if ((flags & MLA_APPEND_RMSNORM) && !(eps >= 0.f)) return MLA_ERR_INVALID_ARG;
-    if ((flags & MLA_APPEND_ROPE) && !(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
     AppendArgs a;
+    if (flags & MLA_APPEND_ROPE) {
+        if (!rope || !rope_frequencies(*rope, cache->d_r, a.theta)) return MLA_ERR_INVALID_ARG;
+    } else {
+        for (int i = 0; i < 32; ++i) a.theta[i] = 0.0;
+    }
     a.seq_ids = seq_ids;
     a.positions = positions;
     a.page_table = cache->page_table;
@@ -282,9 +312,22 @@ mla_status_t mla_cache_append(const mla_cache_t* cache, const void* ckv_raw, con
     a.d_r = cache->d_r;
     a.flags = flags;
     a.eps = eps;
-    a.rope_base = rope_base;
     return cuda_status(launch_append(a, ckv_raw, kr_raw, in_dtype, cache->dtype, cache->data,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+mla_status_t mla_cache_append(const mla_cache_t* cache, const void* ckv_raw, const void* kr_raw, int32_t in_dtype,
+                              const float* gamma, float eps, float rope_base, const int32_t* seq_ids,
+                              const int32_t* positions, int32_t T, uint32_t flags, void* stream) {
+    const mla_rope_t rope = {rope_base, 1.f, 1.f, 32.f, 4096};
+    return mla_cache_append_rope(cache, ckv_raw, kr_raw, in_dtype, gamma, eps, &rope, seq_ids, positions, T, flags,
+                                 stream);
+}
+
+float mla_yarn_softmax_scale(float softmax_scale, float yarn_factor, float coef) {
+    if (!(yarn_factor > 1.f)) return softmax_scale;
+    const double m = (double)coef * log((double)yarn_factor) + 1.0;
+    return (float)((double)softmax_scale * m * m);
 }
 
 mla_status_t mla_decode(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B, const void* q_nope,

@@ -6,11 +6,12 @@
 // page, section 2(3).)
 //
 // One warp per token.  The latent part is fp32 arithmetic with one rounding
-// to the cache dtype.  The RoPE frequencies are computed once on the host in
-// fp64; per pair the angle pos * theta_i is formed and reduced modulo 2 pi in
-// fp64 (three operations), and sine and cosine are taken in fp32 of the
-// reduced angle, so large positions keep full accuracy without fp64
-// transcendental functions (slow on this GPU).
+// to the cache dtype.  The RoPE frequencies (plain, or YaRN-adjusted for an
+// extended context) are computed once on the host in fp64; per pair the angle
+// pos * theta_i is formed and reduced modulo 2 pi in fp64 (three operations),
+// and sine and cosine are taken in fp32 of the reduced angle, so large
+// positions keep full accuracy without fp64 transcendental functions (slow
+// on this GPU).
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
@@ -89,12 +90,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 }  // namespace
 
-cudaError_t launch_append(const AppendArgs& args, const void* ckv, const void* kr, int32_t in_dtype,
+cudaError_t launch_append(const AppendArgs& a, const void* ckv, const void* kr, int32_t in_dtype,
                           int32_t cache_dtype, void* cache, cudaStream_t stream) {
-    if (args.T == 0) return cudaSuccess;
-    AppendArgs a = args;
-    for (int32_t i = 0; i < 32; ++i)
-        a.theta[i] = (i < a.d_r / 2) ? pow((double)a.rope_base, -2.0 * (double)i / (double)a.d_r) : 0.0;
+    if (a.T == 0) return cudaSuccess;
     const dim3 grid((a.T + kWarps - 1) / kWarps);
     const dim3 block(kWarps * 32);
     if (in_dtype == 0 && cache_dtype == 0)

@@ -19,9 +19,8 @@ struct AppendArgs {
     int32_t d_r;
     uint32_t flags;
     float eps;
-    float rope_base;
-    // RoPE frequencies theta_i = rope_base^(-2i/d_r), i < d_r/2, in fp64
-    // (filled by launch_append on the host).
+    // RoPE frequency of pair i (i < d_r/2), in fp64, computed on the host:
+    // theta_i = base^(-2i/d_r), adjusted by YaRN when the context is extended.
     double theta[32];
 };
 

@@ -113,6 +113,54 @@ MLA_API mla_status_t mla_cache_append(const mla_cache_t* cache,
                               uint32_t flags, void* stream);
 
 /*
+ * RoPE with YaRN context extension (DeepSeek-V2 analysis page, section 3.2
+ * "YaRN extends 4K to 128K").  In MLA only the decoupled RoPE key k^R and the
+ * RoPE queries carry positions, so YaRN acts on those d_r dims alone; the
+ * page gives the extension factor s = 40, alpha = 1, beta = 32 (4K x 40 =
+ * 160K).  Frequency of pair i (the page refers to the published YaRN rule
+ * for the interpolation; that rule is what is implemented):
+ *     theta_i   = base^(-2i/d_r),   r_i = original_max_position * theta_i / (2 pi)
+ *     gamma_i   = clamp((r_i - alpha) / (beta - alpha), 0, 1)
+ *     theta'_i  = theta_i * (gamma_i + (1 - gamma_i) / s)
+ * i.e. pairs that turn more than beta times over the original window keep
+ * their frequency, pairs that turn less than alpha times are interpolated by
+ * 1/s, and a linear ramp joins the two.  yarn_factor = 1 is plain RoPE.
+ */
+typedef struct mla_rope {
+    float base;                     /* RoPE base, e.g. 10000                        */
+    float yarn_factor;              /* s >= 1; 1 = no extension                     */
+    float yarn_alpha;               /* ramp start (turns over the window), 1        */
+    float yarn_beta;                /* ramp end, > yarn_alpha, 32                   */
+    int32_t original_max_position;  /* window before extension, e.g. 4096 (>= 1)   */
+} mla_rope_t;
+
+/*
+ * mla_cache_append_rope -- mla_cache_append with the RoPE frequencies of
+ * `rope` (host pointer, read during the call).  Arguments and errors as
+ * mla_cache_append; MLA_ERR_INVALID_ARG also for base <= 0, yarn_factor < 1,
+ * yarn_beta <= yarn_alpha or original_max_position < 1 when
+ * MLA_APPEND_ROPE is set.  mla_cache_append(..., rope_base, ...) equals this
+ * call with yarn_factor = 1.
+ */
+MLA_API mla_status_t mla_cache_append_rope(const mla_cache_t* cache,
+                              const void* ckv_raw, const void* kr_raw, int32_t in_dtype,
+                              const float* gamma, float eps, const mla_rope_t* rope,
+                              const int32_t* seq_ids, const int32_t* positions, int32_t T,
+                              uint32_t flags, void* stream);
+
+/*
+ * mla_yarn_softmax_scale -- softmax scale of a YaRN-extended model.  YaRN's
+ * attention temperature sqrt(1/t) = coef * ln(s) + 1 (coef = 0.0707 in
+ * DeepSeek-V2, 0.1 in the original YaRN; the page's "sqrt(t)" is a typo for
+ * sqrt(1/t)) scales q and k each in the original, i.e. the logits by 1/t.
+ * Because only d_r of the dims carry RoPE in MLA, the temperature is moved
+ * onto the softmax scale: returns softmax_scale * (coef * ln(s) + 1)^2
+ * (s = 40: factor 1.2608^2 = 1.590).  s <= 1 returns softmax_scale.
+ * Host-only arithmetic; no device work.
+ */
+MLA_API float mla_yarn_softmax_scale(float softmax_scale, float yarn_factor, float coef);
+
+/*
  * mla_decode -- absorbed MLA attention of Q query tokens per sequence.
  *
  *  seq_lens [B] int32 (device): cached tokens of each sequence, INCLUDING

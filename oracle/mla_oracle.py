@@ -97,18 +97,55 @@ def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(ms + eps) * np.asarray(gamma, dtype=np.float64)
 
 
-def rope_angles(pos, d_r: int, base: float) -> np.ndarray:
-    """phi[..., i] = pos * base^(-2i/d_r) for the pair (2i, 2i+1)."""
+def rope_theta(d_r: int, base: float) -> np.ndarray:
+    """theta_i = base^(-2i/d_r) for the pairs i < d_r/2."""
     i = np.arange(d_r // 2, dtype=np.float64)
-    theta = np.power(float(base), -2.0 * i / d_r)
+    return np.power(float(base), -2.0 * i / d_r)
+
+
+def yarn_theta(d_r: int, base: float, factor: float, alpha: float, beta: float,
+               original_max_position: int) -> np.ndarray:
+    """RoPE frequencies after YaRN context extension.
+
+    Page "02 · DeepSeek-V2 analysis", section 3.2: YaRN stretches the window
+    from 4K to 128K (factor s = 40, alpha = 1, beta = 32) and, in MLA, acts
+    only on the d_r RoPE dims.  The page defers the interpolation rule to
+    YaRN itself; this is YaRN's by-parts rule: a pair that turns
+    r = L * theta / (2 pi) times over the original window L keeps its
+    frequency when r > beta, is divided by s when r < alpha, and in between
+    blends the two with weight g = (r - alpha) / (beta - alpha).
+    """
+    theta = rope_theta(d_r, base)
+    if factor == 1.0:
+        return theta
+    turns = float(original_max_position) * theta / (2.0 * math.pi)
+    g = np.clip((turns - alpha) / (beta - alpha), 0.0, 1.0)
+    return theta * g + (theta / factor) * (1.0 - g)
+
+
+def yarn_temperature(factor: float, coef: float) -> float:
+    """sqrt(1/t) = coef * ln(s) + 1 (section 3.2: coef 0.0707 in V2, 0.1 in YaRN)."""
+    return coef * math.log(factor) + 1.0 if factor > 1.0 else 1.0
+
+
+def yarn_softmax_scale(scale: float, factor: float, coef: float) -> float:
+    """The temperature moved onto the softmax scale: the original scales q and
+    k each by sqrt(1/t), i.e. the logits by 1/t = sqrt(1/t)^2 (section 3.2)."""
+    m = yarn_temperature(factor, coef)
+    return scale * m * m
+
+
+def rope_angles(pos, d_r: int, base: float, theta=None) -> np.ndarray:
+    """phi[..., i] = pos * theta_i for the pair (2i, 2i+1); theta_i = base^(-2i/d_r) unless given."""
+    theta = rope_theta(d_r, base) if theta is None else np.asarray(theta, dtype=np.float64)
     return np.asarray(pos, dtype=np.float64)[..., None] * theta
 
 
-def rope(x: np.ndarray, pos, base: float) -> np.ndarray:
+def rope(x: np.ndarray, pos, base: float, theta=None) -> np.ndarray:
     """Rotate each dimension pair (2i, 2i+1) of x by the angle pos*theta_i."""
     x = np.asarray(x, dtype=np.float64)
     d_r = x.shape[-1]
-    phi = rope_angles(pos, d_r, base)
+    phi = rope_angles(pos, d_r, base, theta)
     c, s = np.cos(phi), np.sin(phi)
     x0, x1 = x[..., 0::2], x[..., 1::2]
     y = np.empty_like(x)
@@ -121,19 +158,19 @@ APPEND_RMSNORM = 1
 APPEND_ROPE = 2
 
 
-def append_rows(c_raw, k_raw, positions, gamma, eps, base, flags, cache_dtype):
+def append_rows(c_raw, k_raw, positions, gamma, eps, base, flags, cache_dtype, theta=None):
     """The 576-element cache rows [c_kv || k_R] of new tokens.
 
     c_raw [T, d_c] and k_raw [T, d_r] are the raw projections (already widened
     to float64).  The row is computed in float64 and rounded once to the
-    cache dtype.
+    cache dtype.  `theta` overrides the RoPE frequencies (YaRN).
     """
     c = np.asarray(c_raw, dtype=np.float64)
     k = np.asarray(k_raw, dtype=np.float64)
     if flags & APPEND_RMSNORM:
         c = rmsnorm(c, gamma, eps)
     if flags & APPEND_ROPE:
-        k = rope(k, positions, base)
+        k = rope(k, positions, base, theta)
     return round_to_dtype(np.concatenate([c, k], axis=-1), cache_dtype)
 
 

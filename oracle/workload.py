@@ -28,26 +28,29 @@ def workload_scale(w) -> float:
     return softmax_scale(w.d_h, w.d_r)
 
 
-def sequence_cache(w, b: int, s0: int = 0, s1: int | None = None):
-    """Oracle cache rows (C [n, d_c], R [n, d_r], float64) of tokens s0..s1-1 of b."""
+def sequence_cache(w, b: int, s0: int = 0, s1: int | None = None, theta=None):
+    """Oracle cache rows (C [n, d_c], R [n, d_r], float64) of tokens s0..s1-1 of b
+    (`theta`: RoPE frequencies other than the plain ones, e.g. YaRN's)."""
     s1 = int(w.lens[b]) if s1 is None else s1
     c_raw, k_raw = w.raw_rows(b, s0, s1)
     rows = append_rows(widen(c_raw, w.raw_dtype), widen(k_raw, w.raw_dtype),
                        np.arange(s0, s1), np.ones(w.d_c), w.eps, w.rope_base,
-                       append_flags(w), w.dtype)
+                       append_flags(w), w.dtype, theta)
     return rows[:, :w.d_c], rows[:, w.d_c:]
 
 
-def decode_sequence(w, b: int, cache=None):
-    """(out [Q,H,d_c], lse [Q,H]) of sequence b, float64."""
+def decode_sequence(w, b: int, cache=None, scale=None):
+    """(out [Q,H,d_c], lse [Q,H]) of sequence b, float64 (`scale` overrides the
+    workload's softmax scale)."""
     C, R = sequence_cache(w, b) if cache is None else cache
+    scale = workload_scale(w) if scale is None else scale
     qn, qr = w.queries_of(b)
     qn, qr = widen(qn, w.raw_dtype), widen(qr, w.raw_dtype)
     out = np.zeros((w.Q, w.H, w.d_c))
     lse = np.zeros((w.Q, w.H))
     for j in range(w.Q):
         n = visible_length(int(w.lens[b]), w.Q, j)
-        o, l, _ = decode_row(C[:n], R[:n], qn[j], qr[j], workload_scale(w))
+        o, l, _ = decode_row(C[:n], R[:n], qn[j], qr[j], scale)
         out[j], lse[j] = o, l
     return out, lse
 

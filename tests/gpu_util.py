@@ -29,25 +29,30 @@ def append_flags(mla, w) -> int:
     return (mla.MLA_APPEND_RMSNORM if w.rmsnorm else 0) | mla.MLA_APPEND_ROPE
 
 
-def build_cache(w, device="cuda"):
-    """Upload the raw rows and append them all through mla_cache_append."""
+def build_cache(w, device="cuda", rope=None):
+    """Upload the raw rows and append them all through mla_cache_append
+    (mla_cache_append_rope when RoPE parameters are given)."""
     mla = mla_pkg()
     d = upload(w, device)
     pool = empty_pool(w, device, fill_nan=True)
     cache = mla.Cache(pool, d["page_table"], w.d_c, w.d_r)
-    mla.mla_cache_append(cache, d["raw_c"], d["raw_k"], d["seq_ids"], d["positions"], eps=w.eps,
-                         rope_base=w.rope_base, flags=append_flags(mla, w))
+    if rope is None:
+        mla.mla_cache_append(cache, d["raw_c"], d["raw_k"], d["seq_ids"], d["positions"], eps=w.eps,
+                             rope_base=w.rope_base, flags=append_flags(mla, w))
+    else:
+        mla.mla_cache_append_rope(cache, d["raw_c"], d["raw_k"], d["seq_ids"], d["positions"], rope, eps=w.eps,
+                                  flags=append_flags(mla, w))
     del d["raw_c"], d["raw_k"]
     return cache, d
 
 
-def run_decode(w, cache, d, n_split=None, phases=False):
+def run_decode(w, cache, d, n_split=None, phases=False, scale=None):
     """(out float64 [B,Q,H,d_c], lse float64 [B,Q,H]) from the CUDA path."""
     mla = mla_pkg()
     dt = cache.data.dtype
     out = torch.empty((w.B, w.Q, w.H, w.d_c), dtype=dt, device=cache.data.device)
     lse = torch.empty((w.B, w.Q, w.H), dtype=torch.float32, device=cache.data.device)
-    scale = 1.0 / math.sqrt(w.d_h + w.d_r)
+    scale = 1.0 / math.sqrt(w.d_h + w.d_r) if scale is None else scale
     ws = mla.alloc_workspace(w.B, w.Q, w.H, w.d_c, n_split or 0, cache.data.device)
     if phases:
         ns = n_split or 0
@@ -66,14 +71,17 @@ def run_decode(w, cache, d, n_split=None, phases=False):
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
-def compare(w, out, lse, seqs=None):
-    """Element-wise comparison with the oracle on the listed sequences.
+def compare(w, out, lse, seqs=None, theta=None, scale=None):
+    """Element-wise comparison with the oracle on the listed sequences
+    (`theta`, `scale`: RoPE frequencies and softmax scale other than the
+    workload's plain ones).
 
     Returns a dict of max-abs / rel-L2 errors and asserts the tolerances."""
     seqs = range(w.B) if seqs is None else seqs
     ref_o, ref_l, got_o, got_l = [], [], [], []
     for b in seqs:
-        o, l = O.decode_sequence(w, int(b))
+        cache = None if theta is None else O.sequence_cache(w, int(b), theta=theta)
+        o, l = O.decode_sequence(w, int(b), cache=cache, scale=scale)
         ref_o.append(o)
         ref_l.append(l)
         got_o.append(out[b])

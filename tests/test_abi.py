@@ -119,3 +119,25 @@ def test_append_rejects_bad_arguments_before_launch(mla):
 def test_zero_batch_decode_is_a_no_op(mla):
     c = _cache(mla)
     assert _decode(mla, c, B=0, seq=None, qn=None, qr=None, out=None) == mla.MLA_OK
+
+
+def test_append_rope_rejects_bad_rope_parameters_before_launch(mla):
+    c = _cache(mla)
+    f = mla._lib.mla_cache_append_rope
+
+    def call(rope, flags=3, T=4):
+        return f(ctypes.byref(c), 0x7000, 0x8000, mla.MLA_BF16, None, 1e-6, ctypes.byref(rope) if rope else None,
+                 0x9000, 0xA000, T, flags, None)
+
+    assert call(mla.yarn_rope(base=0.0)) == mla.MLA_ERR_INVALID_ARG
+    assert call(mla.yarn_rope(factor=0.5)) == mla.MLA_ERR_INVALID_ARG
+    assert call(mla.yarn_rope(alpha=32.0, beta=32.0)) == mla.MLA_ERR_INVALID_ARG
+    assert call(mla.yarn_rope(original_max_position=0)) == mla.MLA_ERR_INVALID_ARG
+    assert call(None) == mla.MLA_ERR_INVALID_ARG                    # RoPE requested without parameters
+    assert call(mla.yarn_rope(), T=0) == mla.MLA_OK                # no-op, launches nothing
+    assert call(mla.yarn_rope(), T=-1) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_yarn_softmax_scale_is_host_arithmetic(mla):
+    assert abs(mla.mla_yarn_softmax_scale(1.0, 40.0) - (0.0707 * __import__("math").log(40.0) + 1.0) ** 2) < 1e-6
+    assert mla.mla_yarn_softmax_scale(0.25, 1.0) == 0.25

@@ -68,6 +68,45 @@ def test_append_rope_at_position_edges(positions):
     assert np.array_equal(got[perm[0], 0, 512:], k_raw[0])
 
 
+def test_append_yarn_rope_at_position_edges():
+    """YaRN frequencies (s = 40, alpha = 1, beta = 32, 4K window) at the edges
+    of the original and the extended window."""
+    mla = mla_pkg()
+    positions = [0, 4095, 4096, 65535, 131071, 163839]
+    pages = 163840 // 64
+    perm = synth.permutation(78, 9, pages)
+    pool = torch.full((pages, 64, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pt = torch.from_numpy(perm.reshape(1, pages)).cuda()
+    cache = mla.Cache(pool, pt, 512, 64)
+    T = len(positions)
+    c_raw = synth.normal(6, 1, T * 512, 1 / 24, 0, "bf16").reshape(T, 512)
+    k_raw = synth.normal(6, 2, T * 64, 1 / 24, 0, "bf16").reshape(T, 64)
+    pos = np.array(positions, dtype=np.int32)
+    mla.mla_cache_append_rope(cache, to_torch(c_raw, "bf16"), to_torch(k_raw, "bf16"),
+                              torch.zeros(T, dtype=torch.int32, device="cuda"), torch.from_numpy(pos).cuda(),
+                              mla.yarn_rope())
+    got = pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    theta = O.yarn_theta(64, 10000.0, 40.0, 1.0, 32.0, 4096)
+    ref = O.append_rows(O.widen(c_raw, "bf16"), O.widen(k_raw, "bf16"), pos, np.ones(512), 1e-6, 10000.0, 3, "bf16",
+                        theta)
+    for i, p in enumerate(positions):
+        row = got[perm[p // 64], p % 64]
+        ulp = np.abs(_ordered(row) - _ordered(O.f64_to_bf16_bits(ref[i])))
+        assert ulp.max() <= 1, (p, ulp.max())
+    # plain RoPE would differ at large positions: the slow pairs really were interpolated
+    plain = O.append_rows(O.widen(c_raw, "bf16"), O.widen(k_raw, "bf16"), pos, np.ones(512), 1e-6, 10000.0, 3, "bf16")
+    assert not np.array_equal(O.f64_to_bf16_bits(plain[-1]), got[perm[positions[-1] // 64], positions[-1] % 64])
+
+
+def test_bf16_decode_over_a_yarn_cache_with_the_temperature():
+    mla = mla_pkg()
+    w = synth.custom_bf16("yarn_decode", 707, [300, 4100, 70, 2048], H=128, Q=1, paged=True, q_gain=4.0)
+    cache, d = build_cache(w, rope=mla.yarn_rope())
+    scale = mla.mla_yarn_softmax_scale(1.0 / math.sqrt(w.d_h + w.d_r), 40.0)
+    out, lse = run_decode(w, cache, d, scale=scale)
+    compare(w, out, lse, theta=O.yarn_theta(64, 10000.0, 40.0, 1.0, 32.0, 4096), scale=scale)
+
+
 # -------------------------------------------------------------- fp32 path --
 
 @pytest.mark.parametrize("n_split", [None, 2, 4, 64])
