@@ -12,6 +12,7 @@ reported alongside.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
   python bench.py --profile-attend N   # build, plan once, N attention launches, no timing (for ncu)
+  python bench.py --workload long_split # another configuration (default: full_width, the headline)
 """
 from __future__ import annotations
 
@@ -143,8 +144,10 @@ class OracleStep:
         import numpy as np
         import oracle as O
         self.w, self.seqs, self.O, self.np = w, list(seqs), O, np
-        self.caches = {b: O.sequence_cache(w, b, 0, int(w.lens[b]) - w.Q) for b in self.seqs}
-        self.raw_new = {b: w.raw_rows(b, int(w.lens[b]) - w.Q, int(w.lens[b])) for b in self.seqs}
+        first_new = {b: max(0, int(w.lens[b]) - w.Q) for b in self.seqs}
+        self.caches = {b: O.sequence_cache(w, b, 0, first_new[b]) for b in self.seqs}
+        self.raw_new = {b: w.raw_rows(b, first_new[b], int(w.lens[b])) for b in self.seqs}
+        self.first_new = first_new
         try:
             from threadpoolctl import threadpool_info
             self.cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
@@ -156,7 +159,7 @@ class OracleStep:
         for b in self.seqs:
             c_raw, k_raw = self.raw_new[b]
             L = int(w.lens[b])
-            rows = O.append_rows(O.widen(c_raw, w.raw_dtype), O.widen(k_raw, w.raw_dtype), np.arange(L - w.Q, L),
+            rows = O.append_rows(O.widen(c_raw, w.raw_dtype), O.widen(k_raw, w.raw_dtype), np.arange(self.first_new[b], L),
                                  np.ones(w.d_c), w.eps, w.rope_base, O.append_flags(w), w.dtype)
             C = np.concatenate([self.caches[b][0], rows[:, :w.d_c]])
             R = np.concatenate([self.caches[b][1], rows[:, w.d_c:]])
@@ -239,7 +242,8 @@ def run_cuda(args, w):
     del d["raw_c"], d["raw_k"]
     out = torch.empty((w.B, w.Q, w.H, w.d_c), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Q, w.H), dtype=torch.float32, device=dev)
-    ws = mla.alloc_workspace(w.B, w.Q, w.H, w.d_c, 0, dev)
+    n_split = args.n_split
+    ws = mla.alloc_workspace(w.B, w.Q, w.H, w.d_c, n_split, dev)
     scale = 1.0 / math.sqrt(w.d_h + w.d_r)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -250,13 +254,14 @@ def run_cuda(args, w):
     # the event pairs bracket the replays on the same stream.
     def pre():
         mla.mla_cache_append(cache, new_c, new_k, new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
-        mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws)
+        mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws, n_split=n_split)
 
     def attend():
-        mla.mla_decode_attend(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, ws, lse=lse, softmax_scale=scale)
+        mla.mla_decode_attend(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, ws, lse=lse, n_split=n_split,
+                              softmax_scale=scale)
 
     def post():
-        mla.mla_decode_combine(cache, out, ws, lse=lse)
+        mla.mla_decode_combine(cache, out, ws, lse=lse, n_split=n_split)
 
     launches_per_step = 4  # append, plan, attend, combine
 
@@ -337,8 +342,12 @@ def run_cuda(args, w):
 
     def compute(i):
         mla.mla_cache_append(cache, d_c[i], d_k[i], new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
-        mla.mla_decode(cache, d["seq_lens"], d_qn[i], d_qr[i], d_out[i], lse=d_lse[i], workspace=ws,
-                       softmax_scale=scale)
+        if n_split:
+            mla.mla_decode_split_combine(cache, d["seq_lens"], d_qn[i], d_qr[i], d_out[i], n_split, lse=d_lse[i],
+                                         workspace=ws, softmax_scale=scale)
+        else:
+            mla.mla_decode(cache, d["seq_lens"], d_qn[i], d_qr[i], d_out[i], lse=d_lse[i], workspace=ws,
+                           softmax_scale=scale)
 
     with torch.cuda.stream(s_comp):
         for i in range(n_sets):      # eager warm-up of both buffer sets
@@ -415,7 +424,8 @@ def run_cuda(args, w):
         bound = "hbm" if t_mem >= t_tc else "tensor"
         achieved_gbs = alg_bytes / att_avg_s / 1e9
         achieved_tf = flops / att_avg_s / 1e12
-        traffic = kernel_traffic("decode_tc_full_width.md", "head_latent_attention_27_b300/csrc/decode_tc.cu")
+        traffic = (kernel_traffic("decode_tc_full_width.md", "head_latent_attention_27_b300/csrc/decode_tc.cu")
+                   if w.name.startswith("full_width") else None)
         if bound == "hbm":
             roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                     "frac": achieved_gbs / hbm, "traffic": traffic}
@@ -426,23 +436,30 @@ def run_cuda(args, w):
                      "kernel_ms": att_avg_s * 1e3, "alg_bytes": alg_bytes, "alg_flops": flops,
                      "roofline_ms": max(t_mem, t_tc) * 1e3, "frac_of_roofline": max(t_mem, t_tc) / att_avg_s,
                      "tensor_frac": achieved_tf / tc_peak})
-        seqs = list(range(w.B))
+        # oracle sample: whole sequences, at most ~300K cached tokens of fp64 history
+        seqs, tok = [], 0
+        for b in range(w.B):
+            if seqs and tok + int(w.lens[b]) > 300_000:
+                break
+            seqs.append(b)
+            tok += int(w.lens[b])
         cpu_v, cores, cpu_el, cpu_steps = oracle_throughput(w, seqs, budget_s=10.0)
         clocks = clk.summary()
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "S": int(w.lens[0]), "H": w.H, "Q": w.Q, "d_c": w.d_c,
-                       "d_r": w.d_r, "page_size": 64, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "config": {"workload": w.name, "B": w.B, "S": int(w.lens[0]) if len(set(w.lens.tolist())) == 1 else
+                       f"ragged, mean {float(np.mean(w.lens)):.0f}, max {int(np.max(w.lens))}", "H": w.H, "Q": w.Q,
+                       "d_c": w.d_c, "d_r": w.d_r, "page_size": 64, "n_split": n_split, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "l2": "flushed between steps (write > 2x L2 outside the per-step event pairs); "
-                             "cache 302 MB > L2"},
+                             f"cache {cache_bytes / 1e6:.0f} MB > L2"},
             "cache_read_gbs": cache_bytes / step_s / 1e9,
             "tflops": flops / step_s / 1e12,
             "step_roofline_frac": max(t_mem, t_tc) / step_s,
             "roofline": roof,
             "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"all {w.B} sequences, newest token appended + decoded, "
+                             "sample": f"sequences 0..{len(seqs) - 1} of {w.B}, newest token appended + decoded, "
                                        f"{cpu_steps} pass(es) in {cpu_el:.1f} s"},
             "e2e": {"value": world * tokens_per_step / (e2e_tot * 1e-3 / args.steps), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -490,13 +507,19 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", default="full_width", choices=["full_width", "small_head", "ragged_paged",
+                                                                    "long_split"])
+    ap.add_argument("--n-split", type=int, default=None,
+                    help="uniform split of every sequence (default: 64 for long_split, else the balanced plan)")
     ap.add_argument("--profile-attend", type=int, default=0, metavar="N",
                     help="run N attention launches on one plan and exit (no timing; for ncu)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "cuda":
         args.warmup = 3
     import synth
-    w = synth.full_width()
+    w = getattr(synth, args.workload)()
+    if args.n_split is None:
+        args.n_split = 64 if args.workload == "long_split" else 0
     if args.profile_attend > 0:
         run_profile_attend(w, args.profile_attend)
         return
