@@ -131,21 +131,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// P = 2^(s*scale_log2 - m) for the 32 columns [C0, C0+32) of a row, packed
-// to bf16 pairs; returns their fp32 sum.  (Compile-time column offset keeps
-// the score array in registers.)
-template <int C0>
-__device__ __forceinline__ float exp_half(const float (&s)[BN], float scale_log2, float neg_mref,
-                                          uint32_t (&pk)[BN / 4]) {
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int c = 0; c < BN / 2; c += 2) {
-        const float p0 = fast_exp2(fmaf(s[C0 + c], scale_log2, neg_mref));   // exp2(-inf) = 0
-        const float p1 = fast_exp2(fmaf(s[C0 + c + 1], scale_log2, neg_mref));
-        ls[(c >> 1) & 3] += p0 + p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
-    }
-    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+// Packed fp32 pairs (f32x2 add / fma, each lane rounded to nearest like its
+// scalar form) and the three-input max: fewer instructions in the per-tile
+// softmax, whose issue rate and instruction-cache footprint bound the tile
+// period.
+// (x, y) += (a, b)
+__device__ __forceinline__ void add2_to(float& x, float& y, float a, float b) {
+    asm("{\n\t.reg .b64 p, q;\n\tmov.b64 p, {%0, %1};\n\tmov.b64 q, {%2, %3};\n\t"
+        "add.rn.f32x2 p, p, q;\n\tmov.b64 {%0, %1}, p;\n\t}"
+        : "+f"(x), "+f"(y) : "f"(a), "f"(b));
+}
+// (x*a + c, y*b + d)
+__device__ __forceinline__ float2 fma2(float x, float y, float a, float b, float c, float d) {
+    float2 r;
+    asm("{\n\t.reg .b64 p, q, w;\n\tmov.b64 p, {%2, %3};\n\tmov.b64 q, {%4, %5};\n\tmov.b64 w, {%6, %7};\n\t"
+        "fma.rn.f32x2 p, p, q, w;\n\tmov.b64 {%0, %1}, p;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "f"(x), "f"(y), "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
@@ -343,8 +350,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t tS = tmem + TM_S + 64u * slot;
                 const uint32_t sk = sbase + OFF_KV + qk_stage * STAGE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {  // 256 latent dims, A = q_nope from TMEM
+                // 256 latent dims, A = q_nope from TMEM; unrolled by one 64-dim
+                // box (4 MMAs): measured faster than full unrolling (smaller
+                // issue loop) and than unrolling by 1 or 2 (issue overhead)
+#pragma unroll 4
+                for (int kk = 0; kk < 16; ++kk) {
                     const uint64_t bd = smem_desc(sk + (kk >> 2) * KN_BLK + (kk & 3) * 32, 16, 1024, kSwizzle128B);
                     umma_ts(tS, tQ + kk * 8, bd, IDESC_QK, kk != 0 ? 1u : 0u);
                 }
@@ -513,10 +523,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint4 u = xb[c ^ rsw];
                     const float2 f0 = unpack_f16x2(u.x), f1 = unpack_f16x2(u.y);
                     const float2 f2 = unpack_f16x2(u.z), f3 = unpack_f16x2(u.w);
-                    s[8 * c + 0] += f0.x; s[8 * c + 1] += f0.y;
-                    s[8 * c + 2] += f1.x; s[8 * c + 3] += f1.y;
-                    s[8 * c + 4] += f2.x; s[8 * c + 5] += f2.y;
-                    s[8 * c + 6] += f3.x; s[8 * c + 7] += f3.y;
+                    add2_to(s[8 * c + 0], s[8 * c + 1], f0.x, f0.y);
+                    add2_to(s[8 * c + 2], s[8 * c + 3], f1.x, f1.y);
+                    add2_to(s[8 * c + 4], s[8 * c + 5], f2.x, f2.y);
+                    add2_to(s[8 * c + 6], s[8 * c + 7], f3.x, f3.y);
                 }
             }
             __syncwarp();
@@ -528,9 +538,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < BN; ++c) s[c] = (tok0 + c < vis) ? s[c] : -INFINITY;
             }
-            float mx[4] = {s[0], s[1], s[2], s[3]};
+            float mx[4];
 #pragma unroll
-            for (int c = 4; c < BN; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+            for (int k2 = 0; k2 < 4; ++k2) mx[k2] = fmaxf(s[2 * k2], s[2 * k2 + 1]);
+#pragma unroll
+            for (int c = 8; c < BN; c += 8) {
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) mx[k2] = max3f(mx[k2], s[c + 2 * k2], s[c + 2 * k2 + 1]);
+            }
             const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
             // 4. running maximum after tile g-1 (the other group's), lazy
             //    update: O is rescaled only when the max grows by > 2^8
@@ -562,14 +577,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float neg_m = (m_cur == -INFINITY) ? 0.f : -m_cur;
                 uint8_t* prow = smem + OFF_P + slot * P_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                const float sl2 = a.scale_log2;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t w[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float p0 = fast_exp2(fmaf(s[8 * c + 2 * i], a.scale_log2, neg_m));   // exp2(-inf) = 0
-                        const float p1 = fast_exp2(fmaf(s[8 * c + 2 * i + 1], a.scale_log2, neg_m));
-                        ls[i] += p0 + p1;
+                        const float2 x = fma2(s[8 * c + 2 * i], s[8 * c + 2 * i + 1], sl2, sl2, neg_m, neg_m);
+                        const float p0 = fast_exp2(x.x);   // exp2(-inf) = 0
+                        const float p1 = fast_exp2(x.y);
+                        add2_to(ls[2 * (i & 1)], ls[2 * (i & 1) + 1], p0, p1);
                         w[i] = pack_bf16x2(p0, p1);
                     }
                     *reinterpret_cast<uint4*>(prow + ((c ^ rsw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
