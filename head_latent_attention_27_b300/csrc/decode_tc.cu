@@ -290,7 +290,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     bulk_prefetch_l2(cache_bytes + (int64_t)page * (BN * 1152) + rank * (BN * 576), BN * 576);
                 pf.next();
             };
-            for (int32_t i = 0; i < a.prefetch_tiles; ++i) prefetch_next();
+            if constexpr (kTcPrefetchTiles > 0)
+                for (int32_t i = 0; i < a.prefetch_tiles; ++i) prefetch_next();
             for (int32_t p = p_begin; p < p_end && ok; ++p) {
                 const Piece pc = v.pieces[p];
                 const int32_t b = pc.unit / RB, rb = pc.unit % RB;
@@ -305,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         atomicCAS(status, 0, 1);
                         page = 0;
                     }
-                    prefetch_next();
+                    if constexpr (kTcPrefetchTiles > 0) prefetch_next();
                     ok = bounded_wait(bar(B_KVEMPTY + stage), phase ^ 1u, abort_flag, status);
                     if (!ok) break;
                     const uint32_t fb = bar(B_KVFULL + stage);
@@ -324,6 +325,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+#pragma unroll 1
             for (int s = 0; s < NSTAGE; ++s)
                 if (issued_mask & (1u << s)) drain_wait(bar(B_KVFULL + s), (last_parity >> s) & 1u);
             if (q_cnt > 0) drain_wait(bar(B_QRFULL), (q_cnt - 1) & 1u);
