@@ -251,10 +251,18 @@ def run_cuda(args, w):
 
     # The step's launches are captured once in CUDA graphs (append+plan,
     # attend, combine) so that host launch overhead does not starve the GPU;
-    # the event pairs bracket the replays on the same stream.
+    # the event pairs bracket the replays on the same stream.  The plan reads
+    # only seq_lens, so it runs on a side stream beside the append (two
+    # branches of the graph) and the attention waits for both.
+    s_side = torch.cuda.Stream(dev)
+
     def pre():
+        cur = torch.cuda.current_stream(dev)
+        s_side.wait_stream(cur)
+        with torch.cuda.stream(s_side):
+            mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws, n_split=n_split)
         mla.mla_cache_append(cache, new_c, new_k, new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
-        mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws, n_split=n_split)
+        cur.wait_stream(s_side)
 
     def attend():
         mla.mla_decode_attend(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, ws, lse=lse, n_split=n_split,
@@ -341,13 +349,16 @@ def run_cuda(args, w):
     s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def compute(i):
+        # plan beside the append (it reads only seq_lens), then attend + combine
+        cur = torch.cuda.current_stream(dev)
+        s_side.wait_stream(cur)
+        with torch.cuda.stream(s_side):
+            mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws, n_split=n_split)
         mla.mla_cache_append(cache, d_c[i], d_k[i], new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
-        if n_split:
-            mla.mla_decode_split_combine(cache, d["seq_lens"], d_qn[i], d_qr[i], d_out[i], n_split, lse=d_lse[i],
-                                         workspace=ws, softmax_scale=scale)
-        else:
-            mla.mla_decode(cache, d["seq_lens"], d_qn[i], d_qr[i], d_out[i], lse=d_lse[i], workspace=ws,
-                           softmax_scale=scale)
+        cur.wait_stream(s_side)
+        mla.mla_decode_attend(cache, d["seq_lens"], d_qn[i], d_qr[i], d_out[i], ws, lse=d_lse[i], n_split=n_split,
+                              softmax_scale=scale)
+        mla.mla_decode_combine(cache, d_out[i], ws, lse=d_lse[i], n_split=n_split)
 
     with torch.cuda.stream(s_comp):
         for i in range(n_sets):      # eager warm-up of both buffer sets

@@ -31,50 +31,66 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int64_t grow = (int64_t)b * QH + (int64_t)rb * kRowsPerUnit + row;
 
     const float* lp = v.lse_part + (int64_t)p0 * kRowsPerUnit + row;   // lse of piece k: lp[k * 128]
+    // the lse of the first kCached pieces are loaded together (independent
+    // loads in flight), the rest, if any, one by one
+    constexpr int kCached = 8;
+    float lc[kCached];
+#pragma unroll
+    for (int k = 0; k < kCached; ++k) lc[k] = k < n ? lp[(int64_t)k * kRowsPerUnit] : -INFINITY;
     float m = -INFINITY;
-    for (int32_t k = 0; k < n; ++k) m = fmaxf(m, lp[(int64_t)k * kRowsPerUnit]);
+#pragma unroll
+    for (int k = 0; k < kCached; ++k) m = fmaxf(m, lc[k]);
+    for (int32_t k = kCached; k < n; ++k) m = fmaxf(m, lp[(int64_t)k * kRowsPerUnit]);
     float total_lse = -INFINITY;
     if (m != -INFINITY) {
         float z = 0.f;
-        for (int32_t k = 0; k < n; ++k) z += expf(lp[(int64_t)k * kRowsPerUnit] - m);
+#pragma unroll
+        for (int k = 0; k < kCached; ++k) z += k < n ? expf(lc[k] - m) : 0.f;
+        for (int32_t k = kCached; k < n; ++k) z += expf(lp[(int64_t)k * kRowsPerUnit] - m);
         total_lse = m + logf(z);
     }
-    // out = sum_k w_k o_k with w_k = exp(lse_k - lse); the weights of the
-    // first kCached pieces are computed once per row
-    constexpr int kCached = 8;
+    // out = sum_k w_k o_k with w_k = exp(lse_k - lse)
     float wc[kCached];
 #pragma unroll
-    for (int k = 0; k < kCached; ++k) {
-        const float lk = k < n ? lp[(int64_t)k * kRowsPerUnit] : -INFINITY;
-        wc[k] = (total_lse != -INFINITY && lk != -INFINITY) ? expf(lk - total_lse) : 0.f;
-    }
+    for (int k = 0; k < kCached; ++k)
+        wc[k] = (total_lse != -INFINITY && lc[k] != -INFINITY) ? expf(lc[k] - total_lse) : 0.f;
     const float* ob = v.o_part + ((int64_t)p0 * kRowsPerUnit + row) * d_c;   // piece k: ob + k * 128 * d_c
     const int64_t pstride = (int64_t)kRowsPerUnit * d_c;
     // each lane owns up to 4 chunks of 4 columns (d_c <= 512, a multiple of
-    // 4); all of a piece's loads are issued before they are used
+    // 4); the loads of two pieces are issued before either is used
     constexpr int kChunks = 4;
     float4 acc[kChunks];
 #pragma unroll
     for (int j = 0; j < kChunks; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int32_t k = 0; k < n; ++k) {
-        float w;
-        if (k < kCached) {
-            w = wc[k];
-        } else {
-            const float lk = lp[(int64_t)k * kRowsPerUnit];
-            w = (total_lse != -INFINITY && lk != -INFINITY) ? expf(lk - total_lse) : 0.f;
-        }
-        if (w == 0.f) continue;
-        float4 x[kChunks];
+    // acc += w0 o_k0 + w1 o_k1, with both pieces' loads issued before use
+    auto accumulate2 = [&](int32_t k0, float w0, int32_t k1, float w1) {
+        float4 x0[kChunks], x1[kChunks];
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
             const int32_t c0 = lane * 4 + 128 * j;
-            x[j] = c0 < d_c ? *reinterpret_cast<const float4*>(ob + k * pstride + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const bool in = c0 < d_c;
+            x0[j] = in && w0 != 0.f ? *reinterpret_cast<const float4*>(ob + k0 * pstride + c0)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            x1[j] = in && w1 != 0.f ? *reinterpret_cast<const float4*>(ob + k1 * pstride + c0)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
-            acc[j].x += w * x[j].x; acc[j].y += w * x[j].y; acc[j].z += w * x[j].z; acc[j].w += w * x[j].w;
+            acc[j].x += w0 * x0[j].x + w1 * x1[j].x;
+            acc[j].y += w0 * x0[j].y + w1 * x1[j].y;
+            acc[j].z += w0 * x0[j].z + w1 * x1[j].z;
+            acc[j].w += w0 * x0[j].w + w1 * x1[j].w;
         }
+    };
+#pragma unroll
+    for (int k = 0; k < kCached; k += 2) {   // compile-time k: the weights stay in registers
+        if (k >= n) break;
+        accumulate2(k, wc[k], k + 1 < n ? k + 1 : k, k + 1 < n ? wc[k + 1] : 0.f);
+    }
+    for (int32_t k = kCached; k < n; ++k) {
+        const float lk = lp[(int64_t)k * kRowsPerUnit];
+        const float w = (total_lse != -INFINITY && lk != -INFINITY) ? expf(lk - total_lse) : 0.f;
+        accumulate2(k, w, k, 0.f);
     }
 #pragma unroll
     for (int j = 0; j < kChunks; ++j) {
