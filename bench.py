@@ -13,6 +13,7 @@ reported alongside.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
   python bench.py --profile-attend N   # build, plan once, N attention launches, no timing (for ncu)
   python bench.py --workload long_split # another configuration (default: full_width, the headline)
+  python bench.py --absorb              # the absorption GEMMs either side of the decode (own JSON line)
 """
 from __future__ import annotations
 
@@ -512,6 +513,61 @@ def run_profile_attend(w, n: int) -> None:
         raise RuntimeError(f"kernel status {mla.mla_status_string(status)}")
 
 
+def run_absorb(args) -> None:
+    """The two absorption GEMMs at the full-width decode's shape (n = B*Q = 64
+    query rows, H = 128, d_h = 128, d_c = 512): q_nope = W^UK_h^T q^C_h and
+    o = W^UV_h u_h, each timed alone with CUDA events, L2 flushed before every
+    launch (the 16.8 MB weights fit in L2).  Prints one JSON line."""
+    import numpy as np
+    import torch
+
+    import head_latent_attention_27_b300 as mla
+    import synth
+    from synth.device import to_torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n, H, d_h, d_c = 64, 128, 128, 512
+    bf = lambda shape, st, sc: to_torch(synth.normal(2024, st, int(np.prod(shape)), sc, 0, "bf16").reshape(shape),
+                                        "bf16", device=dev)
+    w_uk, w_uv = bf((H, d_h, d_c), 1, 1 / math.sqrt(d_h)), bf((H, d_h, d_c), 2, 1 / math.sqrt(d_c))
+    q_c, u = bf((n, H, d_h), 3, 1.0), bf((n, H, d_c), 4, 1.0)
+    q_nope = torch.empty((n, H, d_c), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((n, H, d_h), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    res = {}
+    for name, fn, x, y in (("absorb_query", mla.mla_absorb_query, (w_uk, q_c), q_nope),
+                           ("absorb_output", mla.mla_absorb_output, (w_uv, u), o)):
+        for _ in range(max(3, args.warmup)):
+            fn(*x, y, status=status)
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn(*x, y, status=status)
+            b.record()
+            ts.append((a, b))
+        torch.cuda.synchronize(dev)
+        us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in ts)
+        alg_bytes = sum(t.numel() * t.element_size() for t in (*x, y))
+        flops = 2 * n * H * d_h * d_c
+        res[name] = {"us": us, "alg_bytes": alg_bytes, "achieved_gbs": alg_bytes / us * 1e-3,
+                     "frac_hbm": alg_bytes / us * 1e-3 / hbm, "tflops": flops / us * 1e-6}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"absorb kernel status {int(status.item())}")
+    line = {"metric": "absorption GEMMs (W^UK into the query, W^UV after the aggregation), GB/s vs HBM roofline",
+            "config": {"workload": "full_width absorption", "n_rows": n, "H": H, "d_h": d_h, "d_c": d_c,
+                       "dtype": "bf16", "l2": "flushed before every launch"},
+            "steps": args.steps, "peak_hbm_gbs": hbm, "peak_source": src, **res}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -524,7 +580,13 @@ def main():
                     help="uniform split of every sequence (default: 64 for long_split, else the balanced plan)")
     ap.add_argument("--profile-attend", type=int, default=0, metavar="N",
                     help="run N attention launches on one plan and exit (no timing; for ncu)")
+    ap.add_argument("--absorb", action="store_true",
+                    help="time the two absorption GEMMs at the full-width shape instead (own JSON line)")
     args = ap.parse_args()
+    if args.absorb:
+        args.steps = min(args.steps, 200)
+        run_absorb(args)
+        return
     if args.warmup < 3 and args.impl == "cuda":
         args.warmup = 3
     import synth

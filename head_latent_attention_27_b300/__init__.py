@@ -71,6 +71,8 @@ _SIGS = {
     "mla_decode_read_status": (_i32, [_vp, _sz, _vp, ctypes.POINTER(_i32)]),
     "mla_selftest_bounded_wait": (_i32, [_vp, _sz, _u32, _vp]),
     "mla_decode_noalloc": (_i32, [_pc, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp]),
+    "mla_absorb_query": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "mla_absorb_output": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "mla_status_string": (ctypes.c_char_p, [_i32]),
     "mla_version": (_i32, []),
 }
@@ -295,6 +297,31 @@ def mla_decode_noalloc(cache: Cache, seq_lens, q_nope, q_rope, out, lse=None,
     cc = cache.c()
     _check(_lib.mla_decode_noalloc(ctypes.byref(cc), _ptr(seq_lens), B, _ptr(q_nope), _ptr(q_rope), Q, H,
                                    float(scale), _ptr(out), _ptr(lse), _stream(stream)), "mla_decode_noalloc")
+
+
+def _absorb_args(w, x, y, d_in: int, d_out: int):
+    torch = _torch()
+    for t, name in ((w, "weights"), (x, "input"), (y, "output")):
+        _need(t, name, torch.bfloat16, 3)
+    H, d_h, d_c = w.shape
+    n = x.shape[0]
+    if tuple(x.shape) != (n, H, (d_h, d_c)[d_in]) or tuple(y.shape) != (n, H, (d_h, d_c)[d_out]):
+        raise ValueError("shapes do not match the weights [H, d_h, d_c]")
+    return n, H, d_h, d_c
+
+
+def mla_absorb_query(w_uk, q_c, q_nope, status=None, stream=None) -> None:
+    """q_nope[n, h, :] = W^UK[h]^T q_c[n, h, :]  (w_uk [H, d_h, d_c], q_c [n, H, d_h])."""
+    n, H, d_h, d_c = _absorb_args(w_uk, q_c, q_nope, 0, 1)
+    _check(_lib.mla_absorb_query(_ptr(w_uk), _ptr(q_c), _ptr(q_nope), n, H, d_h, d_c, _ptr(status),
+                                 _stream(stream)), "mla_absorb_query")
+
+
+def mla_absorb_output(w_uv, u, o, status=None, stream=None) -> None:
+    """o[n, h, :] = W^UV[h] u[n, h, :]  (w_uv [H, d_h, d_c], u [n, H, d_c])."""
+    n, H, d_h, d_c = _absorb_args(w_uv, u, o, 1, 0)
+    _check(_lib.mla_absorb_output(_ptr(w_uv), _ptr(u), _ptr(o), n, H, d_h, d_c, _ptr(status), _stream(stream)),
+           "mla_absorb_output")
 
 
 def mla_decode_read_status(workspace, stream=None) -> int:

@@ -7,6 +7,7 @@
 
 #include <mutex>
 
+#include "absorb.cuh"
 #include "append.cuh"
 #include "decode_f32.cuh"
 #include "decode_plan.cuh"
@@ -79,6 +80,54 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D bf16 tensor map over a row-major [d2][d1][d0] array, box
+// box0 x box1 x box2 (elements along d0 innermost).
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1,
+               uint32_t box2, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The two absorption GEMMs share one kernel; `query_side` selects
+// q_nope = W^UK_h^T q^C_h (reduction over d_h) or o = W^UV_h u_h (over d_c).
+mla_status_t run_absorb(const void* w, const void* x, void* y, int32_t n_rows, int32_t H, int32_t d_h, int32_t d_c,
+                        int32_t* status, void* stream, bool query_side) {
+    if (n_rows < 0 || H < 1 || d_h < 1 || d_c < 1) return MLA_ERR_INVALID_ARG;
+    if (d_h % kAbsorbBM != 0 || d_c % kAbsorbBM != 0 || H > 65535) return MLA_ERR_UNSUPPORTED;
+    if (n_rows > 65535 * kAbsorbBN || (int64_t)n_rows * H * (d_c > d_h ? d_c : d_h) > ((int64_t)1 << 40))
+        return MLA_ERR_UNSUPPORTED;
+    if (n_rows == 0) return MLA_OK;
+    if (!w || !x || !y) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 1u) != 0) return MLA_ERR_INVALID_ARG;
+    const int32_t k_total = query_side ? d_h : d_c;
+    const int32_t m_total = query_side ? d_c : d_h;
+    CUtensorMap tm_a, tm_b;
+    // weights: [H * d_h][d_c] row-major; the query side reads 64 (m) x 64 (k)
+    // boxes (A contiguous along m), the output side 64 (k) x 128 (m) boxes
+    const bool ok_a = query_side ? encode_2d(&tm_a, w, (uint64_t)H * d_h, d_c, d_c, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
+                                 : encode_2d(&tm_a, w, (uint64_t)H * d_h, d_c, d_c, 64, 128,
+                                             CU_TENSOR_MAP_SWIZZLE_128B);
+    // activations: [n_rows][H][k_total], 64 rows of one head per box
+    const bool ok_b = encode_3d(&tm_b, x, k_total, H, n_rows, 64, 1, kAbsorbBN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok_a || !ok_b) return MLA_ERR_CUDA;
+    AbsorbArgs a;
+    a.out = y;
+    a.n_rows = n_rows;
+    a.H = H;
+    a.m_total = m_total;
+    a.k_total = k_total;
+    a.status = status;
+    return launch_absorb(tm_a, tm_b, a, query_side, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
+                                                                                                      : MLA_ERR_CUDA;
+}
 
 mla_status_t check_cache(const mla_cache_t* c) {
     if (!c || !c->data || !c->page_table) return MLA_ERR_INVALID_ARG;
@@ -409,6 +458,16 @@ mla_status_t mla_selftest_bounded_wait(void* workspace, size_t workspace_bytes, 
     if (timeout_us == 0 || timeout_us > 10000000u) return MLA_ERR_INVALID_ARG;
     selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<int*>(workspace), timeout_us);
     return cuda_status(cudaGetLastError());
+}
+
+mla_status_t mla_absorb_query(const void* w_uk, const void* q_c, void* q_nope, int32_t n_rows, int32_t H,
+                              int32_t d_h, int32_t d_c, int32_t* status, void* stream) {
+    return run_absorb(w_uk, q_c, q_nope, n_rows, H, d_h, d_c, status, stream, true);
+}
+
+mla_status_t mla_absorb_output(const void* w_uv, const void* u, void* o, int32_t n_rows, int32_t H, int32_t d_h,
+                               int32_t d_c, int32_t* status, void* stream) {
+    return run_absorb(w_uv, u, o, n_rows, H, d_h, d_c, status, stream, false);
 }
 
 const char* mla_status_string(mla_status_t s) {

@@ -283,6 +283,35 @@ MLA_API mla_status_t mla_decode_noalloc(const mla_cache_t* cache, const int32_t*
                                         float softmax_scale, void* out, float* lse, void* stream);
 
 /* Static description of a status code. */
+/*
+ * Absorption GEMMs either side of the attention ("02 · DeepSeek-V2
+ * analysis", section 1.2, the paragraph on absorbing W^UK into the query, and
+ * section 6.1, where each head aggregates the latents with its own weights
+ * and W^UV is applied afterwards).  bf16 in and out, fp32 accumulation on
+ * the tensor cores.
+ *
+ *  mla_absorb_query:  q_nope[n][h][:] = W^UK[h]^T q_c[n][h][:]
+ *      w_uk   [H][d_h][d_c]   (the up-projection of keys, per head)
+ *      q_c    [n_rows][H][d_h] content queries
+ *      q_nope [n_rows][H][d_c] absorbed queries, the input of mla_decode
+ *  mla_absorb_output: o[n][h][:] = W^UV[h] u[n][h][:]
+ *      w_uv   [H][d_h][d_c]   (the up-projection of values, per head)
+ *      u      [n_rows][H][d_c] aggregated latents, the output of mla_decode
+ *      o      [n_rows][H][d_h] per-head attention outputs (W^O is applied
+ *             by the caller)
+ *
+ *  All arrays are dense row-major device memory owned by the caller; w and
+ *  the activation input must be 16-byte aligned.  d_h and d_c must be
+ *  multiples of 128 (MLA_ERR_UNSUPPORTED otherwise); n_rows = 0 is a no-op.
+ *  status: NULL or a device int32 that receives MLA_ERR_TIMEOUT if an
+ *  in-kernel wait ran out (the kernel then stops cleanly; the output is
+ *  undefined).  Asynchronous on `stream`.
+ */
+MLA_API mla_status_t mla_absorb_query(const void* w_uk, const void* q_c, void* q_nope, int32_t n_rows,
+                                      int32_t H, int32_t d_h, int32_t d_c, int32_t* status, void* stream);
+MLA_API mla_status_t mla_absorb_output(const void* w_uv, const void* u, void* o, int32_t n_rows,
+                                       int32_t H, int32_t d_h, int32_t d_c, int32_t* status, void* stream);
+
 MLA_API const char* mla_status_string(mla_status_t status);
 
 /* Library version as major*10000 + minor*100 + patch. */

@@ -297,6 +297,27 @@ def explicit_mha_row(C, R, qc, qr, W_UK, W_UV):
     return np.stack(outs)
 
 
+def absorb_query(W_UK, q_c):
+    """W^UK absorbed into the query (section 1.2, the absorption paragraph):
+    q_nope[..., h, :] = W^UK_h^T q^C_h, so that q_h^T k_{s,h} = q_nope_h^T c_s.
+
+    W_UK [H, d_h, d_c] (k^C_{s,h} = W_UK[h] @ c_s), q_c [..., H, d_h].
+    Returns [..., H, d_c] (float64).
+    """
+    return np.einsum("hdc,...hd->...hc", np.asarray(W_UK, dtype=np.float64), np.asarray(q_c, dtype=np.float64))
+
+
+def absorb_output(W_UV, u):
+    """W^UV applied after the latent aggregation (section 6.1): each head
+    first aggregates the latents, u_h = sum_s a_{s,h} c_s, then
+    o_h = W^UV_h u_h.
+
+    W_UV [H, d_h, d_c] (v_{s,h} = W_UV[h] @ c_s), u [..., H, d_c].
+    Returns [..., H, d_h] (float64).
+    """
+    return np.einsum("hdc,...hc->...hd", np.asarray(W_UV, dtype=np.float64), np.asarray(u, dtype=np.float64))
+
+
 # ----------------------------------------------------------------------------
 # Cache accounting (section 1.1, 1.3 and 6.2 of the DeepSeek-V2 analysis page)
 # ----------------------------------------------------------------------------

@@ -141,3 +141,22 @@ def test_append_rope_rejects_bad_rope_parameters_before_launch(mla):
 def test_yarn_softmax_scale_is_host_arithmetic(mla):
     assert abs(mla.mla_yarn_softmax_scale(1.0, 40.0) - (0.0707 * __import__("math").log(40.0) + 1.0) ** 2) < 1e-6
     assert mla.mla_yarn_softmax_scale(0.25, 1.0) == 0.25
+
+
+def test_absorb_rejects_bad_arguments_before_launch(mla):
+    for fn in (mla._lib.mla_absorb_query, mla._lib.mla_absorb_output):
+        def call(w=0x10000, x=0x20000, y=0x30000, n=64, H=128, d_h=128, d_c=512):
+            return fn(w, x, y, n, H, d_h, d_c, None, None)
+
+        assert call(n=0, w=None, x=None, y=None) == mla.MLA_OK      # empty: no launch
+        assert call(n=-1) == mla.MLA_ERR_INVALID_ARG
+        assert call(H=0) == mla.MLA_ERR_INVALID_ARG
+        assert call(d_h=64) == mla.MLA_ERR_UNSUPPORTED               # d_h, d_c multiples of 128
+        assert call(d_c=320) == mla.MLA_ERR_UNSUPPORTED
+        assert call(w=None) == mla.MLA_ERR_INVALID_ARG
+        assert call(x=None) == mla.MLA_ERR_INVALID_ARG
+        assert call(y=None) == mla.MLA_ERR_INVALID_ARG
+        assert call(w=0x10008) == mla.MLA_ERR_INVALID_ARG            # TMA needs 16-byte alignment
+        assert call(x=0x20004) == mla.MLA_ERR_INVALID_ARG
+        assert call(y=0x30001) == mla.MLA_ERR_INVALID_ARG            # bf16 output: 2-byte alignment
+        assert call(n=65535 * 64 + 1) == mla.MLA_ERR_UNSUPPORTED     # grid z limit

@@ -238,10 +238,10 @@ def _absorption_case(scale_override=None, seed=1001):
         C, R = O.sequence_cache(w, b)
         _, qr = w.queries_of(b)
         qr = O.widen(qr, w.raw_dtype)[0]
-        q_nope = np.einsum("hdc,hd->hc", W_UK, qc[b])          # W^UK_h^T q^C_h
+        q_nope = O.absorb_query(W_UK, qc[b])                     # W^UK_h^T q^C_h
         scale = O.softmax_scale(d_h, w.d_r) if scale_override is None else scale_override
         u, _, _ = O.decode_row(C, R, q_nope, qr, scale)
-        absorbed = np.einsum("hdc,hc->hd", W_UV, u)               # W^UV_h u_h
+        absorbed = O.absorb_output(W_UV, u)                      # W^UV_h u_h
         explicit = O.explicit_mha_row(C, R, qc[b], qr, W_UK, W_UV)
         worst = max(worst, float(np.max(np.abs(absorbed - explicit)) / np.max(np.abs(explicit))))
     return worst
@@ -249,6 +249,29 @@ def _absorption_case(scale_override=None, seed=1001):
 
 def test_absorbed_equals_explicit_mha():
     assert _absorption_case() <= 1e-12
+
+
+def test_absorb_functions_against_per_head_products():
+    # the batched forms equal the per-head matrix products written out, and a
+    # transposed weight (the d_h x d_c block used the wrong way round) or a
+    # head mix-up does not pass
+    rng = np.random.default_rng(7)
+    H, d_h, d_c, n = 3, 4, 6, 5
+    W = rng.standard_normal((H, d_h, d_c))
+    qc = rng.standard_normal((n, H, d_h))
+    u = rng.standard_normal((n, H, d_c))
+    q = O.absorb_query(W, qc)
+    o = O.absorb_output(W, u)
+    for t in range(n):
+        for h in range(H):
+            assert np.allclose(q[t, h], W[h].T @ qc[t, h], rtol=1e-14, atol=1e-14)
+            assert np.allclose(o[t, h], W[h] @ u[t, h], rtol=1e-14, atol=1e-14)
+    assert not np.allclose(O.absorb_query(W[::-1], qc), q)
+    # q_h^T (W_UK_h c) = (W_UK_h^T q_h)^T c for every latent c: the absorbed
+    # query gives the same content score as the expanded key
+    c = rng.standard_normal(d_c)
+    for h in range(H):
+        assert abs(qc[0, h] @ (W[h] @ c) - q[0, h] @ c) < 1e-12
 
 
 def test_absorption_check_catches_a_wrong_scale_dimension():
