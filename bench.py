@@ -516,8 +516,9 @@ def run_profile_attend(w, n: int) -> None:
 def run_absorb(args) -> None:
     """The two absorption GEMMs at the full-width decode's shape (n = B*Q = 64
     query rows, H = 128, d_h = 128, d_c = 512): q_nope = W^UK_h^T q^C_h and
-    o = W^UV_h u_h, each timed alone with CUDA events, L2 flushed before every
-    launch (the 16.8 MB weights fit in L2).  Prints one JSON line."""
+    o = W^UV_h u_h, each captured in a CUDA graph and timed alone with CUDA
+    events around the replay, L2 flushed before every launch (the 16.8 MB
+    weights fit in L2).  Prints one JSON line."""
     import numpy as np
     import torch
 
@@ -545,12 +546,16 @@ def run_absorb(args) -> None:
         for _ in range(max(3, args.warmup)):
             fn(*x, y, status=status)
         torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()      # replayed, so host-side set-up is not timed
+        with torch.cuda.graph(g):
+            fn(*x, y, status=status)
+        torch.cuda.synchronize(dev)
         ts = []
         for _ in range(args.steps):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            fn(*x, y, status=status)
+            g.replay()
             b.record()
             ts.append((a, b))
         torch.cuda.synchronize(dev)

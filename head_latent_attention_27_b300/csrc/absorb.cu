@@ -4,11 +4,13 @@
 //                B_h[n][k] = q^C[n][h][k],   D -> q_nope[n][h][m];
 //   output side: A_h[m][k] = W^UV[h][m][k]  (K-major),
 //                B_h[n][k] = u[n][h][k],     D -> o[n][h][m].
-// Grid (m_total / 128, H, ceil(n_rows / 64)); 128 threads: warp 0 lane 0
-// streams 64-wide reduction blocks of A and B by TMA into a 4-stage ring,
-// warp 1 lane 0 issues tcgen05.mma (M=128, N=64, K=16) into a 64-column TMEM
-// accumulator, then all four warps read their TMEM lane quarter and store
-// bf16 rows (rows past n_rows are zero-filled by TMA and not stored).
+// Grid (m_total / 128, H, ceil(n_rows / BN)), BN = 64 query rows per CTA;
+// 128 threads: warp 0 lane 0
+// streams 64-wide reduction blocks of A and B by TMA into a ring of up to 4
+// stages (2 for the query side's 128-deep reduction), warp 1 lane 0 issues
+// tcgen05.mma (M=128, N=BN, K=16) into a TMEM accumulator, then all four
+// warps read their TMEM lane quarter and store bf16 rows (rows past n_rows
+// are zero-filled by TMA and not stored).
 // Every wait is bounded; on a timeout the status word (if given) records
 // MLA_ERR_TIMEOUT and the CTA drains its copies and MMAs before it exits.
 #include <cuda_bf16.h>
@@ -19,17 +21,24 @@
 namespace mla {
 namespace {
 
-constexpr int NST = 4;
+constexpr int NST = 4;                                     // ring depth at most (fewer if K is short)
 constexpr uint32_t A_BYTES = kAbsorbBM * kAbsorbBK * 2;   // 16 KB
-constexpr uint32_t B_BYTES = kAbsorbBN * kAbsorbBK * 2;   // 8 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t OFF_BAR = NST * STAGE_BYTES;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 128 + 1024;      // barriers, TMEM slot, abort flag, alignment slack
-constexpr uint32_t TM_COLS = 64;
+
+template <int BN>
+struct Tile {
+    static constexpr uint32_t B_BYTES = BN * kAbsorbBK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TM_COLS = BN < 32 ? 32 : BN;
+    static_assert(STAGE_BYTES % 1024 == 0, "swizzle atoms stay 1024-aligned");
+};
+
+// barriers, TMEM slot and abort flag after the ring; + alignment slack
+__host__ __device__ constexpr uint32_t smem_bytes(uint32_t stage_bytes, int nst) {
+    return (uint32_t)nst * stage_bytes + 128 + 1024;
+}
 
 enum : int { B_FULL = 0, B_EMPTY = NST, B_DONE = 2 * NST, NUM_BARS };
 static_assert(NUM_BARS * 8 <= 96, "barrier area");
-static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms stay 1024-aligned");
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
                                             int32_t y, int32_t z, uint64_t policy) {
@@ -50,16 +59,19 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-template <bool kAMn>
+template <bool kAMn, int BN>
 __global__ void __launch_bounds__(128, 1)
     absorb_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                  const AbsorbArgs a) {
+                  const AbsorbArgs a, const int nst) {
+    constexpr uint32_t STAGE_BYTES = Tile<BN>::STAGE_BYTES;
+    constexpr uint32_t TM_COLS = Tile<BN>::TM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t mt = blockIdx.x, h = blockIdx.y, nt = blockIdx.z;
     const int32_t kblocks = a.k_total / kAbsorbBK;
+    const uint32_t OFF_BAR = (uint32_t)nst * STAGE_BYTES;
     auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 96);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 100);
@@ -90,7 +102,7 @@ __global__ void __launch_bounds__(128, 1)
         const uint64_t pol_x = l2_policy_evict_last();    // activations: read by every m tile
         uint32_t issued_mask = 0, last_parity = 0;
         for (int32_t kb = 0; kb < kblocks; ++kb) {
-            const uint32_t s = (uint32_t)(kb % NST), ph = (uint32_t)(kb / NST) & 1u;
+            const uint32_t s = (uint32_t)(kb % nst), ph = (uint32_t)(kb / nst) & 1u;
             if (!bounded_wait(bar(B_EMPTY + s), ph ^ 1u, abort_flag, a.status)) break;
             const uint32_t full = bar(B_FULL + s);
             const uint32_t dst = sbase + s * STAGE_BYTES;
@@ -102,7 +114,7 @@ __global__ void __launch_bounds__(128, 1)
             } else {      // one box of 64 (k) x 128 (m rows)
                 tma_load_2d(dst, &tm_a, full, kb * kAbsorbBK, h * a.m_total + mt * kAbsorbBM, pol_w);
             }
-            tma_load_3d(dst + A_BYTES, &tm_b, full, kb * kAbsorbBK, h, nt * kAbsorbBN, pol_x);
+            tma_load_3d(dst + A_BYTES, &tm_b, full, kb * kAbsorbBK, h, nt * BN, pol_x);
             issued_mask |= 1u << s;
             last_parity = (last_parity & ~(1u << s)) | (ph << s);
         }
@@ -110,9 +122,9 @@ __global__ void __launch_bounds__(128, 1)
             if (issued_mask & (1u << s)) drain_wait(bar(B_FULL + s), (last_parity >> s) & 1u);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16(kAbsorbBM, kAbsorbBN, kAMn ? 1u : 0u, 0u);
+        constexpr uint32_t idesc = idesc_bf16(kAbsorbBM, BN, kAMn ? 1u : 0u, 0u);
         for (int32_t kb = 0; kb < kblocks; ++kb) {
-            const uint32_t s = (uint32_t)(kb % NST), ph = (uint32_t)(kb / NST) & 1u;
+            const uint32_t s = (uint32_t)(kb % nst), ph = (uint32_t)(kb / nst) & 1u;
             if (!bounded_wait(bar(B_FULL + s), ph, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
@@ -137,23 +149,23 @@ __global__ void __launch_bounds__(128, 1)
     // (the outcome is made warp-uniform: tcgen05.ld is warp-collective)
     if (__all_sync(0xffffffffu, bounded_wait(bar(B_DONE), 0, abort_flag, a.status))) {
         tc_fence_after();
-        uint32_t r0[32], r1[32];
         const uint32_t lane_off = ((uint32_t)(warp & 3) * 32u) << 16;
-        tmem_ld32(tmem + lane_off, r0);
-        tmem_ld32(tmem + lane_off + 32, r1);
-        tmem_ld_wait64(r0, r1);
         const int32_t m = mt * kAbsorbBM + warp * 32 + lane;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-        const int32_t n0 = nt * kAbsorbBN;
+        const int32_t n0 = nt * BN;
         const int64_t row_stride = (int64_t)a.H * a.m_total;
         __nv_bfloat16* col = out + (int64_t)h * a.m_total + m;
+        static_assert(BN == 32 || BN == 64, "epilogue reads 32-column groups");
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (n0 + i < a.n_rows) col[(int64_t)(n0 + i) * row_stride] = __float2bfloat16_rn(__uint_as_float(r0[i]));
+        for (int g = 0; g < BN / 32; ++g) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + 32 * g, r);
+            tmem_ld_wait32(r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (n0 + 32 + i < a.n_rows)
-                col[(int64_t)(n0 + 32 + i) * row_stride] = __float2bfloat16_rn(__uint_as_float(r1[i]));
+            for (int i = 0; i < 32; ++i)
+                if (n0 + 32 * g + i < a.n_rows)
+                    col[(int64_t)(n0 + 32 * g + i) * row_stride] = __float2bfloat16_rn(__uint_as_float(r[i]));
+        }
     }
 
     tc_fence_before();
@@ -164,23 +176,30 @@ __global__ void __launch_bounds__(128, 1)
     }
 }
 
+template <bool kAMn, int BN>
+cudaError_t launch_one(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const AbsorbArgs& a, cudaStream_t stream) {
+    const int kblocks = a.k_total / kAbsorbBK;
+    const int nst = kblocks < NST ? kblocks : NST;
+    const uint32_t smem = smem_bytes(Tile<BN>::STAGE_BYTES, nst);
+    cudaError_t e = cudaFuncSetAttribute(absorb_kernel<kAMn, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes(Tile<BN>::STAGE_BYTES, NST));
+    if (e != cudaSuccess) return e;
+    const dim3 grid(a.m_total / kAbsorbBM, a.H, (a.n_rows + BN - 1) / BN);
+    absorb_kernel<kAMn, BN><<<grid, 128, smem, stream>>>(tm_a, tm_b, a, nst);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+int absorb_rows_per_cta(bool) { return 64; }
 
 cudaError_t launch_absorb(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const AbsorbArgs& a, bool a_mn_major,
                           cudaStream_t stream) {
-    const dim3 grid(a.m_total / kAbsorbBM, a.H, (a.n_rows + kAbsorbBN - 1) / kAbsorbBN);
-    if (a_mn_major) {
-        cudaError_t e = cudaFuncSetAttribute(absorb_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        absorb_kernel<true><<<grid, 128, SMEM_BYTES, stream>>>(tm_a, tm_b, a);
-    } else {
-        cudaError_t e = cudaFuncSetAttribute(absorb_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        absorb_kernel<false><<<grid, 128, SMEM_BYTES, stream>>>(tm_a, tm_b, a);
-    }
-    return cudaGetLastError();
+    // query side: K = d_h is short (2 blocks), so a 2-stage ring and 4 CTAs
+    // per SM.  (32 query rows per CTA on the output side, to fill more SMs
+    // at a 64-row batch, measured slower: the extra L2 reads of the weights
+    // cost more than the added CTAs gain.)
+    return a_mn_major ? launch_one<true, 64>(tm_a, tm_b, a, stream) : launch_one<false, 64>(tm_a, tm_b, a, stream);
 }
 
 }  // namespace mla

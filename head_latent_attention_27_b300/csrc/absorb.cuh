@@ -14,8 +14,11 @@
 namespace mla {
 
 constexpr int kAbsorbBM = 128;   // output columns (weight rows) per CTA
-constexpr int kAbsorbBN = 64;    // query rows per CTA
 constexpr int kAbsorbBK = 64;    // reduction block
+
+// Query rows per CTA (the MMA's N); the activation tensor map's box is this
+// tall.
+int absorb_rows_per_cta(bool a_mn_major);
 
 struct AbsorbArgs {
     void* out;          // [n_rows][H][m_total] bf16

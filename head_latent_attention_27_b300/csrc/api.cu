@@ -102,7 +102,8 @@ mla_status_t run_absorb(const void* w, const void* x, void* y, int32_t n_rows, i
                         int32_t* status, void* stream, bool query_side) {
     if (n_rows < 0 || H < 1 || d_h < 1 || d_c < 1) return MLA_ERR_INVALID_ARG;
     if (d_h % kAbsorbBM != 0 || d_c % kAbsorbBM != 0 || H > 65535) return MLA_ERR_UNSUPPORTED;
-    if (n_rows > 65535 * kAbsorbBN || (int64_t)n_rows * H * (d_c > d_h ? d_c : d_h) > ((int64_t)1 << 40))
+    const int32_t rows_per_cta = absorb_rows_per_cta(query_side);
+    if (n_rows > 65535 * rows_per_cta || (int64_t)n_rows * H * (d_c > d_h ? d_c : d_h) > ((int64_t)1 << 40))
         return MLA_ERR_UNSUPPORTED;
     if (n_rows == 0) return MLA_OK;
     if (!w || !x || !y) return MLA_ERR_INVALID_ARG;
@@ -116,7 +117,7 @@ mla_status_t run_absorb(const void* w, const void* x, void* y, int32_t n_rows, i
                                  : encode_2d(&tm_a, w, (uint64_t)H * d_h, d_c, d_c, 64, 128,
                                              CU_TENSOR_MAP_SWIZZLE_128B);
     // activations: [n_rows][H][k_total], 64 rows of one head per box
-    const bool ok_b = encode_3d(&tm_b, x, k_total, H, n_rows, 64, 1, kAbsorbBN, CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool ok_b = encode_3d(&tm_b, x, k_total, H, n_rows, 64, 1, rows_per_cta, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok_a || !ok_b) return MLA_ERR_CUDA;
     AbsorbArgs a;
     a.out = y;
