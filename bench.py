@@ -210,6 +210,24 @@ def run_reference(args, w):
 
 # ---------------------------------------------------------------- CUDA arm --
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    x itself when not distributed."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank_step: int, steps: int, max_total_ms: float) -> float:
+    """Units all ranks processed per second: each of `world` replicas does
+    `units_per_rank_step` units per step; the job takes the slowest rank's
+    total time over `steps` steps."""
+    return world * units_per_rank_step / (max_total_ms * 1e-3 / steps)
+
+
 def run_cuda(args, w):
     import numpy as np
     import torch
@@ -316,11 +334,7 @@ def run_cuda(args, w):
         t_wall = time.perf_counter() - t_wall0
     step_ms = [a.elapsed_time(b) for a, b in ev]
     att_ms = [a.elapsed_time(b) for a, b in ev_att]
-    tot_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), dist, dev)
     status = mla.mla_decode_read_status(ws)
     if status != mla.MLA_OK:
         raise RuntimeError(f"kernel status {mla.mla_status_string(status)}")
@@ -412,11 +426,7 @@ def run_cuda(args, w):
     e2e_t0, e2e_t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     run_pipeline(args.steps, e2e_t0, e2e_t1)
     torch.cuda.synchronize(dev)
-    e2e_tot = e2e_t0.elapsed_time(e2e_t1)
-    if dist is not None:
-        t = torch.tensor([e2e_tot], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_tot = float(t.item())
+    e2e_tot = max_over_ranks(e2e_t0.elapsed_time(e2e_t1), dist, dev)
     # the last step's result came back and matches the device-resident run
     if not (torch.equal(h_out[(args.steps - 1) % n_sets], out.cpu()) and
             torch.equal(h_lse[(args.steps - 1) % n_sets], lse.cpu())):
@@ -428,7 +438,7 @@ def run_cuda(args, w):
         att_avg_s = statistics.mean(att_ms) * 1e-3
         step_s = tot_ms * 1e-3 / args.steps
         tokens_per_step = w.B * w.Q
-        value = world * tokens_per_step / step_s
+        value = whole_job_rate(world, tokens_per_step, args.steps, tot_ms)
         hbm = peaks["hbm_gbs"]
         tc_peak = peaks["bf16_tflops"]
         t_mem = alg_bytes / (hbm * 1e9)
@@ -473,7 +483,7 @@ def run_cuda(args, w):
             "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"sequences 0..{len(seqs) - 1} of {w.B}, newest token appended + decoded, "
                                        f"{cpu_steps} pass(es) in {cpu_el:.1f} s"},
-            "e2e": {"value": world * tokens_per_step / (e2e_tot * 1e-3 / args.steps), "unit": UNIT,
+            "e2e": {"value": whole_job_rate(world, tokens_per_step, args.steps, e2e_tot), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i (two buffer sets)"},
             "gpu_launches": launches_per_step * args.steps,
