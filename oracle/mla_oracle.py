@@ -297,6 +297,40 @@ def explicit_mha_row(C, R, qc, qr, W_UK, W_UV):
     return np.stack(outs)
 
 
+def prefill_expanded(C, R, qc, qr, W_UK, W_UV, positions, scale=None):
+    """Expanded (prefill) form of the same attention (section 1.2 eq 10-11,
+    1.3 eq 14-18; section 6: prefill materialises K and V, decode absorbs).
+
+    Per head h the keys k_{s,h} = [W_UK_h c_s || R_s] and values
+    v_{s,h} = W_UV_h c_s of the whole sequence are materialised; query t
+    (content qc[t, h], RoPE part qr[t, h], at position positions[t]) attends
+    causally to the keys at positions 0..positions[t], scores divided by
+    sqrt(d_h + d_r) unless `scale` is given.
+    C [S, d_c], R [S, d_r], qc [T, H, d_h], qr [T, H, d_r], W_UK / W_UV
+    [H, d_h, d_c].  Returns o [T, H, d_h] and lse [T, H] (natural log of the
+    sum of exp(scaled score); -inf for a query that sees no key).
+    """
+    C = np.asarray(C, dtype=np.float64)
+    R = np.asarray(R, dtype=np.float64)
+    qc = np.asarray(qc, dtype=np.float64)
+    qr = np.asarray(qr, dtype=np.float64)
+    T, H, d_h = qc.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h + R.shape[1])
+    K_c = np.einsum("sc,hdc->hsd", C, W_UK)                    # [H, S, d_h]
+    V = np.einsum("sc,hdc->hsd", C, W_UV)                      # [H, S, d_h]
+    x = (np.einsum("thd,hsd->ths", qc, K_c) + np.einsum("thr,sr->ths", qr, R)) * scale
+    visible = np.arange(C.shape[0])[None, :] <= np.asarray(positions)[:, None]      # [T, S]
+    x = np.where(visible[:, None, :], x, -np.inf)
+    m = np.max(x, axis=2, keepdims=True)
+    any_key = np.isfinite(m)
+    w = np.exp(x - np.where(any_key, m, 0.0))
+    z = w.sum(axis=2, keepdims=True)
+    o = np.einsum("ths,hsd->thd", w / np.where(any_key, z, 1.0), V)
+    lse = np.where(any_key[..., 0], (m + np.log(np.where(any_key, z, 1.0)))[..., 0], -np.inf)
+    return o, lse
+
+
 def absorb_query(W_UK, q_c):
     """W^UK absorbed into the query (section 1.2, the absorption paragraph):
     q_nope[..., h, :] = W^UK_h^T q^C_h, so that q_h^T k_{s,h} = q_nope_h^T c_s.

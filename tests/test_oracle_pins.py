@@ -274,6 +274,42 @@ def test_absorb_functions_against_per_head_products():
         assert abs(qc[0, h] @ (W[h] @ c) - q[0, h] @ c) < 1e-12
 
 
+def _prefill_case(seed=1002):
+    rng = np.random.default_rng(seed)
+    S, T, H, d_h, d_c, d_r = 24, 5, 3, 8, 32, 4
+    C, R = rng.standard_normal((S, d_c)), rng.standard_normal((S, d_r))
+    W_UK = rng.standard_normal((H, d_h, d_c)) / math.sqrt(d_c)
+    W_UV = rng.standard_normal((H, d_h, d_c)) / math.sqrt(d_c)
+    qc, qr = rng.standard_normal((T, H, d_h)), rng.standard_normal((T, H, d_r))
+    positions = np.array([0, 3, 10, 22, 23])
+    return C, R, qc, qr, W_UK, W_UV, positions
+
+
+def test_expanded_prefill_equals_absorbed_decode_at_every_position():
+    # the prefill (expanded) and decode (absorbed) forms compute one function
+    C, R, qc, qr, W_UK, W_UV, pos = _prefill_case()
+    o, lse = O.prefill_expanded(C, R, qc, qr, W_UK, W_UV, pos)
+    scale = 1 / math.sqrt(qc.shape[2] + R.shape[1])
+    for t, p in enumerate(pos):
+        u, l, _ = O.decode_row(C[:p + 1], R[:p + 1], O.absorb_query(W_UK, qc[t]), qr[t], scale)
+        assert np.allclose(o[t], O.absorb_output(W_UV, u), rtol=1e-12, atol=1e-13)
+        assert np.allclose(lse[t], l, rtol=1e-13)
+        # and equals the per-head explicit form written as loops
+        assert np.allclose(o[t], O.explicit_mha_row(C[:p + 1], R[:p + 1], qc[t], qr[t], W_UK, W_UV),
+                           rtol=1e-12, atol=1e-13)
+
+
+def test_expanded_prefill_is_causal():
+    C, R, qc, qr, W_UK, W_UV, pos = _prefill_case()
+    o, _ = O.prefill_expanded(C, R, qc, qr, W_UK, W_UV, pos)
+    C2, R2 = C.copy(), R.copy()
+    C2[11:] += 5.0                                   # keys after position 10 change
+    R2[11:] -= 3.0
+    o2, _ = O.prefill_expanded(C2, R2, qc, qr, W_UK, W_UV, pos)
+    assert np.array_equal(o[:3], o2[:3])             # queries at 0, 3, 10 do not see them
+    assert not np.allclose(o[3:], o2[3:])
+
+
 def test_absorption_check_catches_a_wrong_scale_dimension():
     # A decode scaled by 1/sqrt(d_c + d_r) (the mismatch the page warns about)
     # must not pass the identity.
