@@ -182,10 +182,20 @@ def oracle_throughput(w, seqs, budget_s: float = 10.0):
     return tokens / el, st.cores, el, passes
 
 
+REFERENCE_BUDGET_S = 150.0   # the reference arm's timed steps end within a few minutes
+
+
 def run_reference(args, w):
     if int(os.environ.get("RANK", "0")) != 0:
         return
-    seqs = list(range(min(4, w.B)))
+    # sample: up to 4 sequences per step, fewer when K steps of 4 would run
+    # past the budget (one pass over one sequence is timed first)
+    probe = OracleStep(w, [0])
+    t0 = time.perf_counter()
+    probe.run()
+    per_seq = time.perf_counter() - t0
+    n_seq = int(max(1, min(4, w.B, REFERENCE_BUDGET_S / max(args.steps * per_seq, 1e-9))))
+    seqs = list(range(n_seq))
     st = OracleStep(w, seqs)
     for _ in range(args.warmup):
         st.run()
