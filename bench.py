@@ -24,9 +24,7 @@ import math
 import os
 import re
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -80,58 +78,109 @@ def kernel_traffic(profile_name: str, src_file: str):
     return float(m.group(1))
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml.so.1 ships with
+    the driver; the Python NVML wheel may be absent)."""
+
+    CLOCK_SM = 1
+    REASONS = (("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20), ("hw_thermal_slowdown", 0x40),
+               ("sw_power_cap", 0x4))
+
+    def __init__(self, device):
+        import ctypes
+        import torch
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        p = torch.cuda.get_device_properties(device)
+        bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h)) != 0:
+            idx = int(getattr(device, "index", 0) or 0)
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(self.h)) != 0:
+                raise RuntimeError("no NVML handle")
+        self._u = ctypes.c_uint()
+        self._ull = ctypes.c_ulonglong()
+
+    def max_sm_mhz(self):
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.ct.byref(self._u)) != 0:
+            return None
+        return float(self._u.value)
+
+    def sample(self):
+        ct = self.ct
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(self._u)) != 0:
+            raise RuntimeError("nvmlDeviceGetClockInfo failed")
+        mhz = float(self._u.value)
+        watts = float("nan")
+        if self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(self._u)) == 0:
+            watts = self._u.value / 1000.0
+        reasons = []
+        if self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(self.h, ct.byref(self._ull)) == 0:
+            r = self._ull.value
+            reasons = [n for n, m in self.REASONS if r & m]
+        return mhz, watts, reasons
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """SM clock, power and clock-event (throttle) reasons sampled about every
+    millisecond during the timed region, by read-only NVML queries from a
+    background thread (the timed region of a short run lasts a few
+    milliseconds, so an nvidia-smi loop at 100 ms would see mostly idle
+    samples)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+    def __init__(self, device):
+        self.device = device
+        self.rows = []
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        self.error = None
 
     def __enter__(self):
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
-        except OSError:
-            self.proc = None
+            nv = _Nvml(self.device)
+            self.max_mhz = nv.max_sm_mhz()
+        except Exception as e:  # pragma: no cover - no NVML on this machine
+            self.error = f"NVML unavailable: {e}"
+            return self
+        self._stop = threading.Event()
+
+        def loop():
+            while not self._stop.is_set():
+                try:
+                    mhz, watts, reasons = nv.sample()
+                except Exception as e:  # pragma: no cover
+                    self.error = str(e)
+                    return
+                self.rows.append((time.perf_counter(), mhz, watts, reasons))
+                time.sleep(0.0005)
+
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
+        time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
 
-    def summary(self):
-        if self.proc is None or not self.path or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
-            except ValueError:
-                continue
-        os.unlink(self.path)
+    def summary(self, t0=None, t1=None):
+        """Median SM clock over the samples taken between t0 and t1
+        (perf_counter times; all samples when none fall inside)."""
+        rows = self.rows
+        if t0 is not None and t1 is not None:
+            inside = [r for r in rows if t0 <= r[0] <= t1]
+            rows = inside or rows
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
-        loaded = [r for r in rows if r[2] > 200.0] or rows
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [self.error or "no samples"]}
+        reasons = sorted({n for r in rows for n in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(r[1] for r in rows), "power_w_max": max(r[2] for r in rows),
+                "samples": len(rows), "sampler": "NVML about every 1 ms, timed region only", "reasons": reasons}
 
 
 # ------------------------------------------------------------------ oracle --
@@ -324,7 +373,7 @@ def run_cuda(args, w):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     ev_att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev) as clk:
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize(dev)
@@ -339,9 +388,10 @@ def run_cuda(args, w):
             ev[i][1].record(stream)
             flush.zero_()          # L2 flush between steps, outside the event pairs
         torch.cuda.synchronize(dev)
+        t_wall1 = time.perf_counter()
         if dist is not None:
             dist.barrier()
-        t_wall = time.perf_counter() - t_wall0
+        t_wall = t_wall1 - t_wall0
     step_ms = [a.elapsed_time(b) for a, b in ev]
     att_ms = [a.elapsed_time(b) for a, b in ev_att]
     tot_ms = max_over_ranks(sum(step_ms), dist, dev)
@@ -476,7 +526,7 @@ def run_cuda(args, w):
             seqs.append(b)
             tok += int(w.lens[b])
         cpu_v, cores, cpu_el, cpu_steps = oracle_throughput(w, seqs, budget_s=10.0)
-        clocks = clk.summary()
+        clocks = clk.summary(t_wall0, t_wall1)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",

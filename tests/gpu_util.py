@@ -71,23 +71,26 @@ def run_decode(w, cache, d, n_split=None, phases=False, scale=None):
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
-def compare(w, out, lse, seqs=None, theta=None, scale=None):
+def compare(w, out, lse, seqs=None, theta=None, scale=None, ref=None):
     """Element-wise comparison with the oracle on the listed sequences
     (`theta`, `scale`: RoPE frequencies and softmax scale other than the
-    workload's plain ones).
+    workload's plain ones; `ref`: the oracle's (out, lse) of those sequences
+    when already computed).
 
     Returns a dict of max-abs / rel-L2 errors and asserts the tolerances."""
-    seqs = range(w.B) if seqs is None else seqs
-    ref_o, ref_l, got_o, got_l = [], [], [], []
-    for b in seqs:
-        cache = None if theta is None else O.sequence_cache(w, int(b), theta=theta)
-        o, l = O.decode_sequence(w, int(b), cache=cache, scale=scale)
-        ref_o.append(o)
-        ref_l.append(l)
-        got_o.append(out[b])
-        got_l.append(lse[b])
-    ref_o, ref_l = np.stack(ref_o), np.stack(ref_l)
-    got_o, got_l = np.stack(got_o), np.stack(got_l)
+    seqs = list(range(w.B) if seqs is None else seqs)
+    if ref is None:
+        ref_o, ref_l = [], []
+        for b in seqs:
+            cache = None if theta is None else O.sequence_cache(w, int(b), theta=theta)
+            o, l = O.decode_sequence(w, int(b), cache=cache, scale=scale)
+            ref_o.append(o)
+            ref_l.append(l)
+        ref_o, ref_l = np.stack(ref_o), np.stack(ref_l)
+    else:
+        ref_o, ref_l = ref
+    got_o = np.stack([out[b] for b in seqs])
+    got_l = np.stack([lse[b] for b in seqs])
     max_abs_t, rel_t, lse_t = tolerances(w.dtype)
     assert np.all(np.isfinite(got_o)), "non-finite output"
     err = np.abs(got_o - ref_o)

@@ -383,3 +383,34 @@ def test_paged_pool_gather_reproduces_sequence_rows():
         C, R = O.sequence_cache(w, b)
         got = O.cache_gather(pool, pt, b, int(w.lens[b]))
         assert np.array_equal(got, np.concatenate([C, R], axis=1))
+
+
+def test_page_slot_against_hand_written_placements():
+    """Token `pos` of sequence `b` lives in page page_table[b][pos // P] at
+    slot pos % P (the cache layout of the C ABI).  The expected (page, slot)
+    pairs below are written out by hand for a 2-sequence table with pages of
+    4 tokens, so a transposed table index or a swapped // and % fails."""
+    pt = np.array([[5, 2, 7], [0, 3, 1]], dtype=np.int32)
+    cases = [  # (seq, pos) -> (page, slot)
+        ((0, 0), (5, 0)), ((0, 3), (5, 3)), ((0, 4), (2, 0)), ((0, 6), (2, 2)),
+        ((0, 9), (7, 1)), ((0, 11), (7, 3)), ((1, 0), (0, 0)), ((1, 5), (3, 1)),
+        ((1, 7), (3, 3)), ((1, 8), (1, 0)), ((1, 10), (1, 2)),
+    ]
+    seq = [c[0][0] for c in cases]
+    pos = [c[0][1] for c in cases]
+    page, slot = O.page_slot(pt, seq, pos, 4)
+    assert [(int(p), int(s)) for p, s in zip(page, slot)] == [c[1] for c in cases]
+    # cache_write puts each row at exactly that place and nowhere else
+    pool = np.full((8, 4, 3), np.nan)
+    rows = np.arange(len(cases) * 3, dtype=np.float64).reshape(len(cases), 3)
+    O.cache_write(pool, pt, seq, pos, rows)
+    for i, (_, (p, s)) in enumerate(cases):
+        assert np.array_equal(pool[p, s], rows[i])
+    assert np.sum(~np.isnan(pool[:, :, 0])) == len(cases)
+    # cache_gather returns a sequence's rows in position order
+    full = np.full((8, 4, 1), np.nan)
+    for b in range(2):
+        for p in range(12):
+            full[pt[b, p // 4], p % 4, 0] = 100 * b + p
+    assert np.array_equal(O.cache_gather(full, pt, 1, 11)[:, 0], 100 + np.arange(11))
+    assert np.array_equal(O.cache_gather(full, pt, 0, 12)[:, 0], np.arange(12))
