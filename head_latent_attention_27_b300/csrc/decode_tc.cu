@@ -25,8 +25,9 @@
 //
 // Pipeline (per CTA, 480 threads):
 //   warp 0      TMA producer: q_rope per piece, 4-stage ring of cache tiles
-//   warp 1      MMA issuer (owns TMEM); QK runs two tiles ahead of PV so the
-//               score swap of tile g+1 overlaps the softmax of tile g
+//   warp 1      QK issuer (owns TMEM): S(g) as soon as tile g has landed and
+//               its score buffer is free, up to two tiles ahead of the
+//               softmax
 //   warps 2-9   softmax, two warpgroups taking alternate tiles (ping-pong):
 //               add the peer's half, online softmax with the running max
 //               handed between the groups, P -> smem, lazy O rescale,
@@ -34,6 +35,11 @@
 //   warp 10     forwards "peer's scores read" to the peer (a slow remote
 //               arrive, kept off the softmax and swap warps)
 //   warps 11-14 score swap: S(g) from TMEM -> fp16 -> st.async to the peer
+//   warp 15     PV issuer: O += P(g) V(g) as soon as P(g) is published, then
+//               frees the cache stage.  QK and PV are issued by different
+//               threads so that a PV whose P is ready never waits behind a
+//               QK whose tile has not landed (with one issuer the stage of
+//               tile g stayed occupied ~4,700 cycles after P(g) was ready).
 // TMEM: O 256 columns | q_nope 128 | S double buffer 2 x 64.
 //
 // Every wait is bounded (ptx.cuh: bounded_wait); on a timeout the kernel
@@ -55,7 +61,8 @@ constexpr int NSTAGE = 4;        // cache-tile ring depth
 constexpr int kSoftmaxWarps = 8;  // two warpgroups
 constexpr int kSwapWarps = 4;
 constexpr int kForwardWarp = 2 + kSoftmaxWarps;                     // warp 10
-constexpr int kThreads = 32 * (3 + kSoftmaxWarps + kSwapWarps);   // 480
+constexpr int kPvWarp = kForwardWarp + 1 + kSwapWarps;             // warp 15
+constexpr int kThreads = 32 * (4 + kSoftmaxWarps + kSwapWarps);   // 512
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_QR = 0;                               // 32 RoPE dims x 128 rows, 64B swizzle
@@ -243,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_PFULL + s), 4);
             mbar_init(bar(B_PVDONE + s), 1);
         }
-        mbar_init(bar(B_EXIT), 1);
+        mbar_init(bar(B_EXIT), 2);   // both MMA issuers commit
         mbar_init(bar(B_OFREE), 4);
         *abort_flag = 0;
         fence_mbar_init_cluster();
@@ -331,14 +338,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (q_cnt > 0) drain_wait(bar(B_QRFULL), (q_cnt - 1) & 1u);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
+        // -------------------------------------------------------- QK issuer
         if (lane == 0) {
-            const uint32_t tO = tmem + TM_O, tQ = tmem + TM_Q;
+            const uint32_t tQ = tmem + TM_Q;
             bool ok = true;
-            TileCursor qk, pv;
+            TileCursor qk;
             qk.init(v.pieces, p_begin, p_end);
-            pv.init(v.pieces, p_begin, p_end);
-            uint32_t g_qk = 0, g_pv = 0, qk_stage = 0, qk_phase = 0, pv_stage = 0, q_cnt = 0, pv_piece = 0;
+            uint32_t g_qk = 0, qk_stage = 0, qk_phase = 0, q_cnt = 0;
 
             auto issue_qk = [&]() -> bool {
                 const uint32_t slot = g_qk & 1u;
@@ -376,6 +382,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 qk.next();
                 return true;
             };
+            while (ok && qk.valid()) ok = issue_qk();
+            umma_commit(bar(B_EXIT));
+            drain_wait(bar(B_EXIT), 0);
+        }
+    } else if (warp == kPvWarp) {
+        // -------------------------------------------------------- PV issuer
+        if (lane == 0) {
+            const uint32_t tO = tmem + TM_O;
+            bool ok = true;
+            TileCursor pv;
+            pv.init(v.pieces, p_begin, p_end);
+            uint32_t g_pv = 0, pv_stage = 0, pv_piece = 0;
             auto issue_pv = [&]() -> bool {
                 const uint32_t slot = g_pv & 1u;
                 if (pv.first() && pv_piece > 0) {
@@ -400,14 +418,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 pv.next();
                 return true;
             };
-            // QK runs up to two tiles ahead of PV, but never into the piece
-            // after next: that piece's q_nope is written by the softmax warps
-            // only once they are past the current piece's epilogue, which
-            // waits for the PV below.
-            while (ok && pv.valid()) {
-                while (ok && qk.valid() && g_qk <= g_pv + 2 && qk.p <= pv.p + 1) ok = issue_qk();
-                if (ok) ok = issue_pv();
-            }
+            while (ok && pv.valid()) ok = issue_pv();
             umma_commit(bar(B_EXIT));
             drain_wait(bar(B_EXIT), 0);
         }
