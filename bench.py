@@ -643,6 +643,88 @@ def run_absorb(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_bench(args) -> None:
+    """The expanded (prefill) form at T = 4096 prompt tokens of one sequence,
+    H = 128 (the full-width decode's per-sequence shape): the up-projection
+    of the cached latents into per-head K^C and V, then the causal attention
+    over [K^C || k^R].  Each phase is timed with CUDA events on the launching
+    stream, the L2 flushed before every step.  Prints one JSON line."""
+    import numpy as np
+    import torch
+
+    import head_latent_attention_27_b300 as mla
+    import synth
+    from synth.device import empty_pool, to_torch, upload
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = synth.prefill(T=args.prefill_tokens, H=128)
+    T, H = int(w.lens[0]), w.H
+    d = upload(w, dev)
+    pool = empty_pool(w, dev, fill_nan=False)
+    cache = mla.Cache(pool, d["page_table"], w.d_c, w.d_r)
+    mla.mla_cache_append(cache, d["raw_c"], d["raw_k"], d["seq_ids"], d["positions"], eps=w.eps,
+                         rope_base=w.rope_base, flags=mla.MLA_APPEND_RMSNORM | mla.MLA_APPEND_ROPE)
+    inp = {k: to_torch(v, "bf16", device=dev) for k, v in synth.prefill_inputs(w).items()}
+    out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(mla.mla_prefill_workspace_size(T, H), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(128 + w.d_r)
+
+    def project():
+        mla.mla_prefill_project(cache, 0, T, inp["w_uk"], inp["w_uv"], ws)
+
+    def attend():
+        mla.mla_prefill_attend(cache, 0, T, inp["q_c"], inp["q_r"], out, ws, lse=lse, softmax_scale=scale)
+
+    for _ in range(max(3, args.warmup)):
+        project()
+        attend()
+    torch.cuda.synchronize(dev)
+    if mla.mla_decode_read_status(ws) != mla.MLA_OK:
+        raise RuntimeError("prefill kernel status not OK")
+    steps = min(args.steps, 50)
+    evs = []
+    with ClockSampler(dev) as clk:
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            project()
+            e[1].record()
+            attend()
+            e[2].record()
+            evs.append(e)
+        torch.cuda.synchronize(dev)
+        t1 = time.perf_counter()
+    if mla.mla_decode_read_status(ws) != mla.MLA_OK:
+        raise RuntimeError("prefill kernel status not OK")
+    proj_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    attn_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+    peaks, src = load_peaks()
+    tc = float(peaks["bf16_tflops"])
+    f_proj = 2.0 * T * w.d_c * 2 * H * 128
+    f_attn = 2.0 * H * (T * (T + 1) / 2) * (128 + w.d_r + 128)
+    line = {
+        "metric": "MLA expanded prefill TFLOP/s vs B300 bf16 roofline",
+        "value": (f_proj + f_attn) / ((proj_ms + attn_ms) * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "tokens_per_s": T / ((proj_ms + attn_ms) * 1e-3), "steps": steps, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "H": H, "d_h": 128, "d_c": w.d_c, "d_r": w.d_r, "causal": True,
+                   "l2": "flushed before every step"},
+        "project": {"kernel": "upproj_kernel", "ms": proj_ms, "flops": f_proj,
+                    "tflops": f_proj / (proj_ms * 1e-3) / 1e12, "frac": f_proj / (proj_ms * 1e-3) / 1e12 / tc},
+        "roofline": {"bound": "tensor", "kernel": "prefill_attn_kernel", "achieved": f_attn / (attn_ms * 1e-3) / 1e12,
+                     "peak": tc, "unit": "TFLOP/s", "frac": f_attn / (attn_ms * 1e-3) / 1e12 / tc,
+                     "kernel_ms": attn_ms, "alg_flops": f_attn, "peak_source": f"{src} burst", "traffic": None},
+        "clocks": clk.summary(t0, t1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -657,7 +739,13 @@ def main():
                     help="run N attention launches on one plan and exit (no timing; for ncu)")
     ap.add_argument("--absorb", action="store_true",
                     help="time the two absorption GEMMs at the full-width shape instead (own JSON line)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the expanded (prefill) form instead: projection + causal attention (own JSON line)")
+    ap.add_argument("--prefill-tokens", type=int, default=4096)
     args = ap.parse_args()
+    if args.prefill:
+        run_prefill_bench(args)
+        return
     if args.absorb:
         args.steps = min(args.steps, 200)
         run_absorb(args)

@@ -73,6 +73,10 @@ _SIGS = {
     "mla_decode_noalloc": (_i32, [_pc, _vp, _i32, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp]),
     "mla_absorb_query": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
     "mla_absorb_output": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "mla_prefill_workspace_size": (_sz, [_i32, _i32]),
+    "mla_prefill_expanded": (_i32, [_pc, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "mla_prefill_project": (_i32, [_pc, _i32, _i32, _vp, _vp, _i32, _vp, _sz, _vp]),
+    "mla_prefill_attend": (_i32, [_pc, _i32, _i32, _vp, _vp, _i32, _f32, _vp, _vp, _vp, _sz, _vp]),
     "mla_status_string": (ctypes.c_char_p, [_i32]),
     "mla_version": (_i32, []),
 }
@@ -322,6 +326,59 @@ def mla_absorb_output(w_uv, u, o, status=None, stream=None) -> None:
     n, H, d_h, d_c = _absorb_args(w_uv, u, o, 1, 0)
     _check(_lib.mla_absorb_output(_ptr(w_uv), _ptr(u), _ptr(o), n, H, d_h, d_c, _ptr(status), _stream(stream)),
            "mla_absorb_output")
+
+
+def mla_prefill_workspace_size(T: int, H: int) -> int:
+    n = _lib.mla_prefill_workspace_size(int(T), int(H))
+    if n == 0:
+        raise RuntimeError("mla_prefill_workspace_size: invalid arguments")
+    return int(n)
+
+
+def mla_prefill_expanded(cache: Cache, seq: int, T: int, w_uk, w_uv, q_c, q_r, out, lse=None, workspace=None,
+                         softmax_scale: float | None = None, stream=None) -> None:
+    """Causal attention of the first T tokens of sequence `seq` in the expanded
+    form: K^C = W^UK c and V = W^UV c materialised per head, keys
+    [K^C || k^R], queries [q_c || q_r] (w_uk / w_uv [H, 128, 512],
+    q_c [T, H, 128], q_r [T, H, 64], out [T, H, 128], lse [T, H])."""
+    torch = _torch()
+    for t, name in ((w_uk, "w_uk"), (w_uv, "w_uv"), (q_c, "q_c"), (q_r, "q_r"), (out, "out")):
+        _need(t, name, torch.bfloat16, 3)
+    H = w_uk.shape[0]
+    if (tuple(w_uk.shape) != (H, 128, cache.d_c) or tuple(w_uv.shape) != (H, 128, cache.d_c) or
+            tuple(q_c.shape) != (T, H, 128) or tuple(q_r.shape) != (T, H, cache.d_r) or
+            tuple(out.shape) != (T, H, 128)):
+        raise ValueError("prefill shapes do not match")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+        if tuple(lse.shape) != (T, H):
+            raise ValueError("lse must be [T, H]")
+    scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(128 + cache.d_r)
+    if workspace is None:
+        workspace = torch.empty(mla_prefill_workspace_size(T, H), dtype=torch.uint8, device=out.device)
+    cc = cache.c()
+    _check(_lib.mla_prefill_expanded(ctypes.byref(cc), int(seq), int(T), _ptr(w_uk), _ptr(w_uv), _ptr(q_c),
+                                     _ptr(q_r), H, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)), "mla_prefill_expanded")
+
+
+def mla_prefill_project(cache: Cache, seq: int, T: int, w_uk, w_uv, workspace, stream=None) -> None:
+    """First phase of mla_prefill_expanded: K^C and V into the workspace."""
+    H = w_uk.shape[0]
+    cc = cache.c()
+    _check(_lib.mla_prefill_project(ctypes.byref(cc), int(seq), int(T), _ptr(w_uk), _ptr(w_uv), H, _ptr(workspace),
+                                    workspace.numel(), _stream(stream)), "mla_prefill_project")
+
+
+def mla_prefill_attend(cache: Cache, seq: int, T: int, q_c, q_r, out, workspace, lse=None,
+                       softmax_scale: float | None = None, stream=None) -> None:
+    """Second phase of mla_prefill_expanded: causal attention over the projected K^C, V."""
+    H = q_c.shape[1]
+    scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(128 + cache.d_r)
+    cc = cache.c()
+    _check(_lib.mla_prefill_attend(ctypes.byref(cc), int(seq), int(T), _ptr(q_c), _ptr(q_r), H, float(scale),
+                                   _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mla_prefill_attend")
 
 
 def mla_decode_read_status(workspace, stream=None) -> int:

@@ -12,6 +12,7 @@
 #include "decode_f32.cuh"
 #include "decode_plan.cuh"
 #include "decode_tc.cuh"
+#include "prefill.cuh"
 #include "mla.h"
 #include "ptx.cuh"
 
@@ -132,13 +133,13 @@ mla_status_t run_absorb(const void* w, const void* x, void* y, int32_t n_rows, i
 
 mla_status_t check_cache(const mla_cache_t* c) {
     if (!c || !c->data || !c->page_table) return MLA_ERR_INVALID_ARG;
-    if (c->dtype != MLA_BF16 && c->dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+    if (c->dtype != MLA_BF16 && c->dtype != MLA_FP32 && c->dtype != MLA_FP8) return MLA_ERR_INVALID_ARG;
     if (c->num_seqs < 1 || c->num_pages < 1 || c->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
     if (c->num_pages > (1 << 24) || (int64_t)c->max_pages_per_seq * kTileTokens > (1 << 30))
         return MLA_ERR_INVALID_ARG;
     if (c->page_size != kTileTokens) return MLA_ERR_UNSUPPORTED;
     if (c->d_c < 1 || c->d_r < 0 || (c->d_r & 1)) return MLA_ERR_INVALID_ARG;
-    if (c->dtype == MLA_BF16) {
+    if (c->dtype == MLA_BF16 || c->dtype == MLA_FP8) {
         if (c->d_c != 512 || c->d_r != 64) return MLA_ERR_UNSUPPORTED;
         if (!aligned16(c->data)) return MLA_ERR_INVALID_ARG;
     } else {
@@ -149,7 +150,7 @@ mla_status_t check_cache(const mla_cache_t* c) {
 }
 
 int32_t num_workers(const DeviceInfo* d, int32_t dtype) {
-    return dtype == MLA_BF16 ? d->tc_clusters : d->sms;
+    return dtype == MLA_FP32 ? d->sms : d->tc_clusters;
 }
 
 struct DecodeShape {
@@ -165,7 +166,7 @@ mla_status_t check_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeS
     if (s.n_split < 0 || s.n_split > kMaxSplit) return MLA_ERR_INVALID_ARG;
     if (s.B > 0 && (!seq_lens || !q_nope || !out || (c->d_r > 0 && !q_rope))) return MLA_ERR_INVALID_ARG;
     if ((int64_t)s.B * s.Q * s.H > (int64_t)1 << 30) return MLA_ERR_UNSUPPORTED;
-    if (c->dtype == MLA_BF16 && s.B > 0 && (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(out)))
+    if (c->dtype != MLA_FP32 && s.B > 0 && (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(out)))
         return MLA_ERR_INVALID_ARG;
     return MLA_OK;
 }
@@ -223,6 +224,7 @@ mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShap
         a.scale = scale;
         return cuda_status(launch_decode_f32(a, P, ws, L, stream));
     }
+    if (c->dtype == MLA_FP8) return MLA_ERR_UNSUPPORTED;   // attention over the low-precision cache: not yet
     TcMaps maps;
     const uint64_t cache_rows = (uint64_t)c->num_pages * kTileTokens;
     const uint64_t qrows = (uint64_t)s.B * s.Q * s.H;
@@ -257,7 +259,9 @@ mla_status_t do_combine(const mla_cache_t* c, DecodeShape s, void* out, float* l
     mla_status_t st = check_workspace(ws, ws_bytes, L);
     if (st != MLA_OK) return st;
     if (s.B == 0) return MLA_OK;
-    return cuda_status(launch_combine(s.B, s.Q, s.H, c->d_c, c->dtype, out, lse, ws, L, stream));
+    // the low-precision cache decodes into bf16 output like the bf16 cache
+    const int32_t out_dtype = c->dtype == MLA_FP32 ? MLA_FP32 : MLA_BF16;
+    return cuda_status(launch_combine(s.B, s.Q, s.H, c->d_c, out_dtype, out, lse, ws, L, stream));
 }
 
 mla_status_t run_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeShape s, const void* q_nope,
@@ -469,6 +473,119 @@ mla_status_t mla_absorb_query(const void* w_uk, const void* q_c, void* q_nope, i
 mla_status_t mla_absorb_output(const void* w_uv, const void* u, void* o, int32_t n_rows, int32_t H, int32_t d_h,
                                int32_t d_c, int32_t* status, void* stream) {
     return run_absorb(w_uv, u, o, n_rows, H, d_h, d_c, status, stream, false);
+}
+
+size_t mla_prefill_workspace_size(int32_t T, int32_t H) {
+    if (T < 0 || H < 1 || (int64_t)T * H > ((int64_t)1 << 31)) return 0;
+    const size_t kv = ws_align((size_t)T * (size_t)H * kPrefillDh * 2);
+    return 256 + 2 * kv;
+}
+
+}  // extern "C"
+
+namespace mla {
+namespace {
+
+enum PrefillPhase { kPrefillProject = 1, kPrefillAttend = 2, kPrefillBoth = 3 };
+
+mla_status_t run_prefill(const mla_cache_t* cache, int32_t seq, int32_t T, const void* w_uk, const void* w_uv,
+                         const void* q_c, const void* q_r, int32_t H, float softmax_scale, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, cudaStream_t s, int phases) {
+    mla_status_t st = check_cache(cache);
+    if (st != MLA_OK) return st;
+    if (cache->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+    if (seq < 0 || seq >= cache->num_seqs || T < 0 || H < 1) return MLA_ERR_INVALID_ARG;
+    if (H % 2 != 0 || H > 4096) return MLA_ERR_UNSUPPORTED;
+    if ((int64_t)T > (int64_t)cache->max_pages_per_seq * kTileTokens) return MLA_ERR_INVALID_ARG;
+    if (!check_scale(softmax_scale)) return MLA_ERR_INVALID_ARG;
+    const size_t need = mla_prefill_workspace_size(T, H);
+    if (need == 0) return MLA_ERR_UNSUPPORTED;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+        return MLA_ERR_WORKSPACE;
+    if (T == 0) return MLA_OK;
+    if ((phases & kPrefillProject) && (!w_uk || !w_uv || !aligned16(w_uk) || !aligned16(w_uv)))
+        return MLA_ERR_INVALID_ARG;
+    if ((phases & kPrefillAttend) &&
+        (!q_c || !q_r || !out || !aligned16(q_c) || !aligned16(q_r) || !aligned16(out)))
+        return MLA_ERR_INVALID_ARG;
+    const DeviceInfo* d = device_info();
+    if (!d || d->err != cudaSuccess || d->sms <= 0) return MLA_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t kv = ws_align((size_t)T * (size_t)H * kPrefillDh * 2);
+    void* k_c = ws + 256;
+    void* v = ws + 256 + kv;
+    int32_t* status = reinterpret_cast<int32_t*>(ws);
+    const uint64_t pool_rows = (uint64_t)cache->num_pages * kTileTokens;
+    const uint64_t n_per = (uint64_t)H * kPrefillDh;
+    const int32_t* page_row = cache->page_table + (int64_t)seq * cache->max_pages_per_seq;
+    const int32_t pages = (T + kTileTokens - 1) / kTileTokens;
+    if (phases & kPrefillProject) {
+        // the status word starts each prefill at zero (the projection runs first)
+        if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
+        UpprojMaps um;
+        if (!encode_2d(&um.latent, cache->data, pool_rows, 576, 576, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&um.w_uk, w_uk, n_per, kPrefillDc, kPrefillDc, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&um.w_uv, w_uv, n_per, kPrefillDc, kPrefillDc, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MLA_ERR_CUDA;
+        UpprojArgs ua;
+        ua.page_row = page_row;
+        ua.pages = pages;
+        ua.num_pages = cache->num_pages;
+        ua.T = T;
+        ua.n_per = (int32_t)n_per;
+        ua.k_out = k_c;
+        ua.v_out = v;
+        ua.status = status;
+        if (launch_upproj(um, ua, d->sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    if (phases & kPrefillAttend) {
+        PrefillAttnMaps am;
+        if (!encode_2d(&am.q_c, q_c, (uint64_t)T, n_per, n_per, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&am.q_r, q_r, (uint64_t)T, (uint64_t)H * kPrefillDr, (uint64_t)H * kPrefillDr, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&am.k_c, k_c, (uint64_t)T, n_per, n_per, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&am.v, v, (uint64_t)T, n_per, n_per, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&am.k_r, cache->data, pool_rows, 576, 576, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MLA_ERR_CUDA;
+        PrefillAttnArgs aa;
+        aa.page_row = page_row;
+        aa.pages = pages;
+        aa.num_pages = cache->num_pages;
+        aa.T = T;
+        aa.H = H;
+        aa.scale_log2 = softmax_scale * 1.4426950408889634f;
+        aa.out = out;
+        aa.lse = lse;
+        aa.status = status;
+        if (launch_prefill_attn(am, aa, d->sms, s) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+extern "C" {
+
+mla_status_t mla_prefill_expanded(const mla_cache_t* cache, int32_t seq, int32_t T, const void* w_uk,
+                                  const void* w_uv, const void* q_c, const void* q_r, int32_t H, float softmax_scale,
+                                  void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    return run_prefill(cache, seq, T, w_uk, w_uv, q_c, q_r, H, softmax_scale, out, lse, workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream), kPrefillBoth);
+}
+
+mla_status_t mla_prefill_project(const mla_cache_t* cache, int32_t seq, int32_t T, const void* w_uk,
+                                 const void* w_uv, int32_t H, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    return run_prefill(cache, seq, T, w_uk, w_uv, nullptr, nullptr, H, 1.f, nullptr, nullptr, workspace,
+                       workspace_bytes, static_cast<cudaStream_t>(stream), kPrefillProject);
+}
+
+mla_status_t mla_prefill_attend(const mla_cache_t* cache, int32_t seq, int32_t T, const void* q_c, const void* q_r,
+                                int32_t H, float softmax_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    return run_prefill(cache, seq, T, nullptr, nullptr, q_c, q_r, H, softmax_scale, out, lse, workspace,
+                       workspace_bytes, static_cast<cudaStream_t>(stream), kPrefillAttend);
 }
 
 const char* mla_status_string(mla_status_t s) {

@@ -65,12 +65,32 @@ typedef enum mla_status {
 
 typedef enum mla_dtype {
     MLA_BF16 = 0,             /* bfloat16 */
-    MLA_FP32 = 1              /* IEEE float32 */
+    MLA_FP32 = 1,             /* IEEE float32 */
+    MLA_FP8 = 2               /* low-precision cache rows (cache only, see below) */
 } mla_dtype_t;
+
+/*
+ * Low-precision cache (dtype MLA_FP8): "02 · DeepSeek-V2 analysis",
+ * sections 1.3 and 6.2, say the deployed cache is quantised further (to
+ * about 6 bits per element) and warn that the quantisation scales must not
+ * mix the axis the absorbed product contracts; the page gives no format.
+ * This library's format: each token's row is 656 bytes,
+ *     bytes [0, 512)    the 512 latent values as FP8 E4M3 codes
+ *                       (OCP "E4M3FN": bias 7, max 448, no infinities),
+ *     bytes [512, 528)  4 fp32 scales, one per 128 consecutive latent values,
+ *     bytes [528, 656)  the 64 RoPE-key values in bf16,
+ * value = E4M3(code) * scale.  The scale runs along one token's latent,
+ * so it commutes with both contractions over tokens.  `data` is then
+ * uint8 [num_pages][page_size][656] (d_c = 512, d_r = 64 only), 16-byte
+ * aligned.  mla_cache_append forms the bf16 row (exactly as for a bf16
+ * cache) and quantises it: s = amax/448 (fp32 division; 1 for an all-zero
+ * group), code = nearest E4M3 (ties to even, saturating) of the
+ * fp32-rounded quotient x/s.
+ */
 
 /* Describes a paged latent cache.  Plain data; the caller owns both arrays. */
 typedef struct mla_cache {
-    void* data;                /* device [num_pages][page_size][d_c + d_r]          */
+    void* data;                /* device [num_pages][page_size][d_c + d_r] (MLA_FP8: [..][656] bytes) */
     const int32_t* page_table; /* device int32 [B][max_pages_per_seq], page ids     */
     int32_t dtype;             /* mla_dtype_t of `data`                             */
     int32_t num_seqs;          /* rows of page_table (sequences addressable)        */
@@ -311,6 +331,56 @@ MLA_API mla_status_t mla_absorb_query(const void* w_uk, const void* q_c, void* q
                                       int32_t H, int32_t d_h, int32_t d_c, int32_t* status, void* stream);
 MLA_API mla_status_t mla_absorb_output(const void* w_uv, const void* u, void* o, int32_t n_rows,
                                        int32_t H, int32_t d_h, int32_t d_c, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Expanded (prefill) attention
+ *
+ * "02 · DeepSeek-V2 analysis", sections 1.2-1.3 (eq 10-11 up-projections,
+ * eq 14-18 decoupled RoPE and the scaled two-part score) and section 6
+ * (prefill may materialise K and V; decode absorbs them; the two forms are
+ * one function in exact arithmetic).  For the first T tokens of sequence
+ * `seq` of the cache (already appended, positions 0..T-1):
+ *
+ *   K^C[t][h] = W^UK[h] c_t,  V[t][h] = W^UV[h] c_t        (materialised)
+ *   o[t][h]   = sum_{s<=t} softmax_s(scale ([q_c[t][h] || q_r[t][h]] .
+ *                                           [K^C[s][h] || k^R_s])) V[s][h]
+ *   lse[t][h] = ln sum_{s<=t} exp(scale * score)
+ *
+ * with c_t the cached latent row (d_c = 512) and k^R_s the cached, rotated
+ * RoPE key (d_r = 64, shared by every head).  Causal: query t sees keys
+ * 0..t.  bf16 cache only; d_h = 128 and H even (MLA_ERR_UNSUPPORTED
+ * otherwise).
+ *
+ *   w_uk, w_uv  bf16 [H][128][512]   per-head key / value up-projections
+ *   q_c         bf16 [T][H][128]     content queries
+ *   q_r         bf16 [T][H][64]      RoPE queries, already rotated at t
+ *   out         bf16 [T][H][128]     per-head outputs (W^O applied by the caller)
+ *   lse         fp32 [T][H] or NULL
+ *   workspace   caller-owned device memory of mla_prefill_workspace_size(T, H)
+ *               bytes, 256-byte aligned: a status word (read it with
+ *               mla_decode_read_status) and the materialised K^C and V.
+ *
+ * All pointers are device memory owned by the caller, 16-byte aligned.
+ * Asynchronous on `stream`; host-side checks return before any launch,
+ * device-side checks (page ids) and in-kernel timeouts are recorded in the
+ * workspace status word.
+ * ---------------------------------------------------------------------- */
+MLA_API size_t mla_prefill_workspace_size(int32_t T, int32_t H);
+MLA_API mla_status_t mla_prefill_expanded(const mla_cache_t* cache, int32_t seq, int32_t T, const void* w_uk,
+                                          const void* w_uv, const void* q_c, const void* q_r, int32_t H,
+                                          float softmax_scale, void* out, float* lse, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+/* The two phases of mla_prefill_expanded, same arguments and workspace:
+ * mla_prefill_project materialises K^C and V in the workspace (and clears
+ * its status word); mla_prefill_attend then runs the causal attention over
+ * them.  A caller that wants the materialised K / V for several query sets
+ * projects once. */
+MLA_API mla_status_t mla_prefill_project(const mla_cache_t* cache, int32_t seq, int32_t T, const void* w_uk,
+                                         const void* w_uv, int32_t H, void* workspace, size_t workspace_bytes,
+                                         void* stream);
+MLA_API mla_status_t mla_prefill_attend(const mla_cache_t* cache, int32_t seq, int32_t T, const void* q_c,
+                                        const void* q_r, int32_t H, float softmax_scale, void* out, float* lse,
+                                        void* workspace, size_t workspace_bytes, void* stream);
 
 MLA_API const char* mla_status_string(mla_status_t status);
 

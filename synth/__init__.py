@@ -277,3 +277,35 @@ WORKLOADS = {
     "ragged_paged": ragged_paged,
     "long_split": long_split,
 }
+
+
+# Prefill (expanded form) draws: the per-head up-projections and the
+# queries of T prompt tokens, each its own stream.
+STREAM_W_UK = 8
+STREAM_W_UV = 9
+STREAM_Q_C = 10
+STREAM_Q_R = 11
+
+
+def prefill(T: int = 4096, H: int = 128, seed: int = 1006, paged: bool = False) -> Workload:
+    """One sequence of T prompt tokens (bf16, d_c=512, d_r=64, d_h=128):
+    raw c_kv ~ N(0,1)/sqrt(576) (RMSNorm'd by the append), raw k_R ~ N(0,1)
+    (rotated at positions 0..T-1 by the append)."""
+    return Workload(f"prefill_T{T}_H{H}", seed, B=1, Q=1, H=H, d_c=512, d_r=64, d_h=128, dtype="bf16",
+                    lens=np.array([T], np.int32), paged=paged, rmsnorm=True, std_c=_std(576), std_k=1.0,
+                    std_qn=_std(576), std_qr=_std(576))
+
+
+def prefill_inputs(w: Workload, heads=None, rows=None) -> dict:
+    """bf16 bits of W^UK, W^UV [H, d_h, d_c] ~ N(0,1)/sqrt(d_c) and of the
+    queries q_c [T, H, d_h], q_r [T, H, d_r] ~ N(0,1) (`heads` / `rows`:
+    draw only those heads of the weights / those query rows)."""
+    T, H, dh, dc, dr = int(w.lens[0]), w.H, w.d_h, w.d_c, w.d_r
+    heads = np.arange(H) if heads is None else np.asarray(heads)
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    wk = np.stack([normal(w.seed, STREAM_W_UK, dh * dc, _std(dc), int(h) * dh * dc, "bf16") for h in heads])
+    wv = np.stack([normal(w.seed, STREAM_W_UV, dh * dc, _std(dc), int(h) * dh * dc, "bf16") for h in heads])
+    qc_idx = (rows[:, None] * H + heads[None, :]).reshape(-1)
+    qc = normal_rows_bf16(w.seed, STREAM_Q_C, qc_idx, dh, 1.0).reshape(len(rows), len(heads), dh)
+    qr = normal_rows_bf16(w.seed, STREAM_Q_R, qc_idx, dr, 1.0).reshape(len(rows), len(heads), dr)
+    return {"w_uk": wk.reshape(len(heads), dh, dc), "w_uv": wv.reshape(len(heads), dh, dc), "q_c": qc, "q_r": qr}

@@ -160,3 +160,39 @@ def test_absorb_rejects_bad_arguments_before_launch(mla):
         assert call(x=0x20004) == mla.MLA_ERR_INVALID_ARG
         assert call(y=0x30001) == mla.MLA_ERR_INVALID_ARG            # bf16 output: 2-byte alignment
         assert call(n=65535 * 64 + 1) == mla.MLA_ERR_UNSUPPORTED     # grid z limit
+
+
+def test_prefill_workspace_size_is_host_arithmetic(mla):
+    # status header (256 B) + K^C and V, each T*H*128 bf16 rounded up to 256 B
+    assert mla._lib.mla_prefill_workspace_size(4096, 128) == 256 + 2 * 4096 * 128 * 128 * 2
+    assert mla._lib.mla_prefill_workspace_size(3, 2) == 256 + 2 * 1536
+    assert mla._lib.mla_prefill_workspace_size(-1, 2) == 0
+    assert mla._lib.mla_prefill_workspace_size(4, 0) == 0
+
+
+def test_prefill_rejects_bad_arguments_before_launch(mla):
+    import ctypes
+    cc = mla.mla_cache_t(0x100000, 0x200000, mla.MLA_BF16, 2, 128, 64, 512, 64, 64)
+    ws_need = mla._lib.mla_prefill_workspace_size(1000, 16)
+
+    def call(cache=cc, seq=0, T=1000, H=16, scale=0.07, ws=0x400000, ws_bytes=ws_need, wk=0x500000, q=0x600000,
+             out=0x700000):
+        return mla._lib.mla_prefill_expanded(ctypes.byref(cache), seq, T, wk, wk, q, q, H, scale, out, None, ws,
+                                             ws_bytes, None)
+
+    assert call(T=0) == mla.MLA_OK                                   # empty: no launch
+    assert call(seq=2) == mla.MLA_ERR_INVALID_ARG                    # beyond the page table's rows
+    assert call(seq=-1) == mla.MLA_ERR_INVALID_ARG
+    assert call(T=64 * 64 + 1) == mla.MLA_ERR_INVALID_ARG            # beyond the sequence's pages
+    assert call(H=15) == mla.MLA_ERR_UNSUPPORTED                     # H even
+    assert call(H=0) == mla.MLA_ERR_INVALID_ARG
+    assert call(scale=0.0) == mla.MLA_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == mla.MLA_ERR_INVALID_ARG
+    assert call(ws=None) == mla.MLA_ERR_WORKSPACE
+    assert call(ws=0x400010) == mla.MLA_ERR_WORKSPACE                # 256-byte alignment
+    assert call(ws_bytes=ws_need - 1) == mla.MLA_ERR_WORKSPACE
+    assert call(wk=None) == mla.MLA_ERR_INVALID_ARG
+    assert call(q=0x600008) == mla.MLA_ERR_INVALID_ARG               # TMA needs 16-byte alignment
+    assert call(out=None) == mla.MLA_ERR_INVALID_ARG
+    fp32 = mla.mla_cache_t(0x100000, 0x200000, mla.MLA_FP32, 2, 128, 64, 64, 16, 64)
+    assert call(cache=fp32) == mla.MLA_ERR_UNSUPPORTED               # bf16 cache only
