@@ -88,6 +88,86 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 }
 
+// Low-precision cache row (656 bytes): the 512 latent values as E4M3 codes,
+// one fp32 scale per 128-element group, then the RoPE key in bf16.  The row
+// is first formed exactly as for the bf16 cache (same arithmetic and
+// reduction order, one rounding to bf16), and those bf16 values are
+// quantised: s = amax / 448 (fp32 division, s = 1 for an all-zero group),
+// code = E4M3(x / s) with the quotient rounded to fp32 first, then to the
+// nearest E4M3 value (ties to even, saturating at +-448).  One warp per
+// token; lane k owns latent elements [16k, 16k + 16), so a group is 8 lanes.
+template <typename Tin>
+__global__ void __launch_bounds__(kWarps * 32)
+    append_fp8_kernel(AppendArgs a, const Tin* __restrict__ ckv, const Tin* __restrict__ kr, uint8_t* __restrict__ cache) {
+    const int32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int32_t lane = threadIdx.x & 31;
+    if (t >= a.T) return;
+    const int32_t b = a.seq_ids[t], pos = a.positions[t];
+    if (b < 0 || b >= a.num_seqs || pos < 0 || pos >= a.max_pages_per_seq * a.page_size) return;
+    const int32_t page = a.page_table[(int64_t)b * a.max_pages_per_seq + pos / a.page_size];
+    if (page < 0 || page >= a.num_pages) return;
+    uint8_t* row = cache + ((int64_t)page * a.page_size + pos % a.page_size) * kFp8RowBytes;
+    const Tin* x = ckv + (int64_t)t * kFp8Dc;
+
+    float inv_rms = 1.f;
+    if (a.flags & 1u) {   // same summation order as the bf16 row
+        float ss = 0.f;
+        for (int32_t k = lane; k < kFp8Dc; k += 32) {
+            const float v = load_f(x + k);
+            ss = fmaf(v, v, ss);
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+        inv_rms = 1.f / sqrtf(ss / (float)kFp8Dc + a.eps);
+    }
+    float y[16];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int32_t k = 16 * lane + i;
+        float v = load_f(x + k);
+        if (a.flags & 1u) v = v * inv_rms * (a.gamma ? a.gamma[k] : 1.f);
+        y[i] = __bfloat162float(__float2bfloat16_rn(v));   // the bf16 row value
+        amax = fmaxf(amax, fabsf(y[i]));
+    }
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t lo, hi;
+        const float q0 = __fdiv_rn(y[4 * j], s), q1 = __fdiv_rn(y[4 * j + 1], s);
+        const float q2 = __fdiv_rn(y[4 * j + 2], s), q3 = __fdiv_rn(y[4 * j + 3], s);
+        asm("{\n\t.reg .b16 h;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n\tcvt.u32.u16 %0, h;\n\t}"
+            : "=r"(lo) : "f"(q0), "f"(q1));
+        asm("{\n\t.reg .b16 h;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n\tcvt.u32.u16 %0, h;\n\t}"
+            : "=r"(hi) : "f"(q2), "f"(q3));
+        w[j] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+    if ((lane & 7) == 0) *reinterpret_cast<float*>(row + kFp8Dc + 4 * (lane >> 3)) = s;
+
+    // shared RoPE key (bf16), as in the bf16 row
+    const Tin* kx = kr + (int64_t)t * a.d_r;
+    __nv_bfloat16* kr_out = reinterpret_cast<__nv_bfloat16*>(row + kFp8Dc + 16);
+    for (int32_t i = lane; i < a.d_r / 2; i += 32) {
+        const float x0 = load_f(kx + 2 * i), x1 = load_f(kx + 2 * i + 1);
+        float y0 = x0, y1 = x1;
+        if (a.flags & 2u) {
+            constexpr double kTwoPi = 6.283185307179586476925286766559;
+            const double ang = (double)pos * a.theta[i];
+            const double r = fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);
+            float sf, cf;
+            sincosf((float)r, &sf, &cf);
+            y0 = x0 * cf - x1 * sf;
+            y1 = x0 * sf + x1 * cf;
+        }
+        kr_out[2 * i] = __float2bfloat16_rn(y0);
+        kr_out[2 * i + 1] = __float2bfloat16_rn(y1);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, const void* ckv, const void* kr, int32_t in_dtype,
@@ -95,6 +175,17 @@ cudaError_t launch_append(const AppendArgs& a, const void* ckv, const void* kr, 
     if (a.T == 0) return cudaSuccess;
     const dim3 grid((a.T + kWarps - 1) / kWarps);
     const dim3 block(kWarps * 32);
+    if (cache_dtype == 2) {   // low-precision (E4M3 latent) rows
+        if (in_dtype == 0)
+            append_fp8_kernel<__nv_bfloat16><<<grid, block, 0, stream>>>(
+                a, static_cast<const __nv_bfloat16*>(ckv), static_cast<const __nv_bfloat16*>(kr),
+                static_cast<uint8_t*>(cache));
+        else
+            append_fp8_kernel<float><<<grid, block, 0, stream>>>(a, static_cast<const float*>(ckv),
+                                                                 static_cast<const float*>(kr),
+                                                                 static_cast<uint8_t*>(cache));
+        return cudaGetLastError();
+    }
     if (in_dtype == 0 && cache_dtype == 0)
         append_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, 0, stream>>>(
             a, static_cast<const __nv_bfloat16*>(ckv), static_cast<const __nv_bfloat16*>(kr),

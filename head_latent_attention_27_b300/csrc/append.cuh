@@ -5,6 +5,13 @@
 
 namespace mla {
 
+// Low-precision cache row: 512 E4M3 latent codes, 4 fp32 group scales (one
+// per 128 latent elements), 64 bf16 RoPE values = 656 bytes.
+constexpr int kFp8Dc = 512;
+constexpr int kFp8Dr = 64;
+constexpr int kFp8Group = 128;
+constexpr int kFp8RowBytes = kFp8Dc + 4 * (kFp8Dc / kFp8Group) + 2 * kFp8Dr;
+
 struct AppendArgs {
     const int32_t* seq_ids;
     const int32_t* positions;

@@ -23,7 +23,11 @@ finite value is 1.75 * 2^8 = 448.  Encoding rounds to nearest, ties to even,
 and saturates finite values beyond +-448 to +-448.
 
 Group scale: s = amax / 448 (amax = largest |x| of the group; s = 1 for an
-all-zero group), rounded to fp32; code = E4M3(x / s); value = E4M3 * s.
+all-zero group), rounded to fp32; code = E4M3(x / s) with the quotient x / s
+rounded to fp32 first (the precision in which the quantising kernel takes
+the same decision: an fp32 division, correctly rounded, then one rounding to
+E4M3); value = E4M3 * s.  (Rounding the float64 quotient of two fp32 numbers
+to fp32 gives the correctly rounded fp32 quotient, since 53 >= 2 * 24 + 2.)
 """
 from __future__ import annotations
 
@@ -76,7 +80,7 @@ def quantize_latent(c, group: int = GROUP):
     g = c.reshape(*c.shape[:-1], d_c // group, group)
     amax = np.max(np.abs(g), axis=-1)
     scale = _round_f32(np.where(amax > 0, amax / E4M3_MAX, 1.0))
-    codes = e4m3_encode(g / scale[..., None])
+    codes = e4m3_encode(_round_f32(g / scale[..., None]))
     return codes.reshape(c.shape), scale
 
 
