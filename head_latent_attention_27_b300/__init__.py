@@ -23,7 +23,8 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE = range(6)
-MLA_BF16, MLA_FP32 = 0, 1
+MLA_BF16, MLA_FP32, MLA_FP8 = 0, 1, 2
+FP8_ROW_BYTES = 656   # low-precision row: 512 E4M3 codes, 4 fp32 group scales, 64 bf16 RoPE values
 MLA_APPEND_RMSNORM = 1
 MLA_APPEND_ROPE = 2
 PAGE_SIZE = 64
@@ -118,6 +119,8 @@ def _dtype_code(t) -> int:
         return MLA_BF16
     if t.dtype == torch.float32:
         return MLA_FP32
+    if t.dtype == torch.uint8:
+        return MLA_FP8
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -137,7 +140,8 @@ def _need(t, name, dtype=None, ndim=None):
 
 @dataclass
 class Cache:
-    """A paged latent cache: data [num_pages, 64, d_c + d_r] and page_table [B, max_pages]."""
+    """A paged latent cache: data [num_pages, 64, d_c + d_r] and page_table [B, max_pages]
+    (a uint8 `data` [num_pages, 64, 656] is the low-precision cache, MLA_FP8)."""
     data: "object"
     page_table: "object"
     d_c: int
@@ -147,8 +151,9 @@ class Cache:
         torch = _torch()
         _need(self.data, "cache.data", ndim=3)
         _need(self.page_table, "cache.page_table", torch.int32, 2)
-        if self.data.shape[1] != PAGE_SIZE or self.data.shape[2] != self.d_c + self.d_r:
-            raise ValueError("cache.data must be [num_pages, 64, d_c + d_r]")
+        width = FP8_ROW_BYTES if self.data.dtype == torch.uint8 else self.d_c + self.d_r
+        if self.data.shape[1] != PAGE_SIZE or self.data.shape[2] != width:
+            raise ValueError(f"cache.data must be [num_pages, 64, {width}]")
 
     def c(self) -> mla_cache_t:
         return mla_cache_t(self.data.data_ptr(), self.page_table.data_ptr(), _dtype_code(self.data),
