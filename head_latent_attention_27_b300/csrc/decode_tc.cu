@@ -162,8 +162,13 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return d;
 }
 
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
-    return __half22float2(*reinterpret_cast<const __half2*>(&u));
+// (x, y) += the two fp16 values packed in u (low half to x), each widened
+// inside a mixed-precision add (fp16 operand, fp32 accumulator and result):
+// no separate conversion instructions.
+__device__ __forceinline__ void add_f16x2_to(float& x, float& y, uint32_t u) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(x), "+f"(y) : "r"(u));
 }
 
 // Bounded wait taken by all 32 lanes; the outcome is made warp-uniform so
@@ -345,6 +350,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             TileCursor qk;
             qk.init(v.pieces, p_begin, p_end);
             uint32_t g_qk = 0, qk_stage = 0, qk_phase = 0, q_cnt = 0;
+            const uint64_t bdesc_nope0 = smem_desc(sbase + OFF_KV, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc_rope0 = smem_desc(sbase + OFF_KV + 4 * KN_BLK, 16, 512, kSwizzle64B);
+            const uint64_t adesc_rope = smem_desc(sbase + OFF_QR, 16, 512, kSwizzle64B);
 
             auto issue_qk = [&]() -> bool {
                 const uint32_t slot = g_qk & 1u;
@@ -357,21 +365,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!bounded_wait(bar(B_SEMPTY + slot), ((g_qk >> 1) & 1u) ^ 1u, abort_flag, status)) return false;
                 tc_fence_after();
                 const uint32_t tS = tmem + TM_S + 64u * slot;
-                const uint32_t sk = sbase + OFF_KV + qk_stage * STAGE_BYTES;
-                // 256 latent dims, A = q_nope from TMEM; unrolled by one 64-dim
-                // box (4 MMAs): measured faster than full unrolling (smaller
-                // issue loop) and than unrolling by 1 or 2 (issue overhead)
-#pragma unroll 4
-                for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t bd = smem_desc(sk + (kk >> 2) * KN_BLK + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-                    umma_ts(tS, tQ + kk * 8, bd, IDESC_QK, kk != 0 ? 1u : 0u);
-                }
+                // Per-MMA descriptors differ from the stage's first one only in
+                // the start-address field (address / 16 in the low 14 bits;
+                // every shared address here is below 2^18, so the add never
+                // carries out of it): one add per MMA.
+                const uint64_t stage_off = (uint64_t)(qk_stage * (STAGE_BYTES >> 4));
+                const uint64_t bn0 = bdesc_nope0 + stage_off;
+                const uint64_t br0 = bdesc_rope0 + stage_off;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {   // 32 RoPE dims, A = q_rope from smem
-                    const uint64_t ad = smem_desc(sbase + OFF_QR + kk * 32, 16, 512, kSwizzle64B);
-                    const uint64_t bd = smem_desc(sk + 4 * KN_BLK + kk * 32, 16, 512, kSwizzle64B);
-                    umma_ss(tS, ad, bd, IDESC_QK, 1u);
-                }
+                for (int kk = 0; kk < 16; ++kk)   // 256 latent dims, A = q_nope from TMEM
+                    umma_ts(tS, tQ + kk * 8, bn0 + (uint64_t)((((kk >> 2) * KN_BLK + (kk & 3) * 32)) >> 4),
+                            IDESC_QK, kk != 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)    // 32 RoPE dims, A = q_rope from smem
+                    umma_ss(tS, adesc_rope + (uint64_t)(kk * 2), br0 + (uint64_t)(kk * 2), IDESC_QK, 1u);
                 umma_commit(bar(B_SFULL + slot));
                 if (qk.last()) umma_commit(bar(B_QREMPTY));
                 ++g_qk;
@@ -394,6 +401,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             TileCursor pv;
             pv.init(v.pieces, p_begin, p_end);
             uint32_t g_pv = 0, pv_stage = 0, pv_piece = 0;
+            const uint64_t bdesc_v0 = smem_desc(sbase + OFF_KV, KN_BLK, 1024, kSwizzle128B);
+            const uint64_t adesc_p0 = smem_desc(sbase + OFF_P, 16, 1024, kSwizzle128B);
             auto issue_pv = [&]() -> bool {
                 const uint32_t slot = g_pv & 1u;
                 if (pv.first() && pv_piece > 0) {
@@ -402,15 +411,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (pv.first()) ++pv_piece;
                 if (!bounded_wait(bar(B_PFULL + slot), (g_pv >> 1) & 1u, abort_flag, status)) return false;
                 tc_fence_after();
-                const uint32_t sk = sbase + OFF_KV + pv_stage * STAGE_BYTES;
-                const uint32_t sp = sbase + OFF_P + slot * P_BYTES;
+                const uint64_t ap0 = adesc_p0 + (uint64_t)(slot * (P_BYTES >> 4));
+                const uint64_t bv0 = bdesc_v0 + (uint64_t)(pv_stage * (STAGE_BYTES >> 4));
                 const bool first = pv.first();
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = smem_desc(sp + kk * 32, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(sk + kk * 2048, KN_BLK, 1024, kSwizzle128B);
-                    umma_ss(tO, ad, bd, IDESC_PV, (first && kk == 0) ? 0u : 1u);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)   // descriptors: start address + offset / 16
+                    umma_ss(tO, ap0 + (uint64_t)(kk * 2), bv0 + (uint64_t)(kk * 128), IDESC_PV,
+                            (first && kk == 0) ? 0u : 1u);
                 umma_commit(bar(B_PVDONE + slot));
                 umma_commit(bar(B_KVEMPTY + pv_stage));
                 ++g_pv;
@@ -534,12 +541,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 u = xb[c ^ rsw];
-                    const float2 f0 = unpack_f16x2(u.x), f1 = unpack_f16x2(u.y);
-                    const float2 f2 = unpack_f16x2(u.z), f3 = unpack_f16x2(u.w);
-                    add2_to(s[8 * c + 0], s[8 * c + 1], f0.x, f0.y);
-                    add2_to(s[8 * c + 2], s[8 * c + 3], f1.x, f1.y);
-                    add2_to(s[8 * c + 4], s[8 * c + 5], f2.x, f2.y);
-                    add2_to(s[8 * c + 6], s[8 * c + 7], f3.x, f3.y);
+                    add_f16x2_to(s[8 * c + 0], s[8 * c + 1], u.x);
+                    add_f16x2_to(s[8 * c + 2], s[8 * c + 3], u.y);
+                    add_f16x2_to(s[8 * c + 4], s[8 * c + 5], u.z);
+                    add_f16x2_to(s[8 * c + 6], s[8 * c + 7], u.w);
                 }
             }
             __syncwarp();
