@@ -44,12 +44,14 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def algorithmic_counts(w):
-    """Bytes the method must move and flops it must do (per decode)."""
+def algorithmic_counts(w, lowp: bool = False):
+    """Bytes the method must move and flops it must do (per decode); `lowp`:
+    the low-precision cache rows (656 bytes per token instead of 1152)."""
     import numpy as np
     elt = 2 if w.dtype == "bf16" else 4
     width = w.d_c + w.d_r
-    cache_bytes = int(np.sum(w.lens.astype(np.int64))) * width * elt
+    row_bytes = 656 if lowp else width * elt
+    cache_bytes = int(np.sum(w.lens.astype(np.int64))) * row_bytes
     q_bytes = w.B * w.Q * w.H * width * elt
     out_bytes = w.B * w.Q * w.H * w.d_c * elt
     visible = 0
@@ -306,7 +308,10 @@ def run_cuda(args, w):
 
     # ---- resident inputs: cache built by the append kernel from raw rows
     d = upload(w, dev)
-    pool = empty_pool(w, dev, fill_nan=False)
+    if args.lowp:   # low-precision cache rows (E4M3 latent, fp32 group scales, bf16 RoPE key)
+        pool = torch.zeros((w.num_pages, 64, mla.FP8_ROW_BYTES), dtype=torch.uint8, device=dev)
+    else:
+        pool = empty_pool(w, dev, fill_nan=False)
     cache = mla.Cache(pool, d["page_table"], w.d_c, w.d_r)
     flags = mla.MLA_APPEND_RMSNORM | mla.MLA_APPEND_ROPE
     mla.mla_cache_append(cache, d["raw_c"], d["raw_k"], d["seq_ids"], d["positions"], eps=w.eps,
@@ -358,6 +363,9 @@ def run_cuda(args, w):
     status = mla.mla_decode_read_status(ws)
     if status != mla.MLA_OK:
         raise RuntimeError(f"kernel status {mla.mla_status_string(status)}")
+    # one graph per step (the timed `value`), and the three phases as graphs
+    # of their own, replayed with an event pair around the attention alone
+    # (its roofline fraction)
     graphs = []
     for fn in (pre, attend, post):
         g = torch.cuda.CUDAGraph()
@@ -365,7 +373,12 @@ def run_cuda(args, w):
             fn()
         graphs.append(g)
     g_pre, g_att, g_post = graphs
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        pre(); attend(); post()
     for _ in range(args.warmup):
+        g_step.replay()
+        flush.zero_()
         g_pre.replay(); g_att.replay(); g_post.replay()
         flush.zero_()
     torch.cuda.synchronize(dev)
@@ -380,11 +393,7 @@ def run_cuda(args, w):
         t_wall0 = time.perf_counter()
         for i in range(args.steps):
             ev[i][0].record(stream)
-            g_pre.replay()
-            ev_att[i][0].record(stream)
-            g_att.replay()
-            ev_att[i][1].record(stream)
-            g_post.replay()
+            g_step.replay()
             ev[i][1].record(stream)
             flush.zero_()          # L2 flush between steps, outside the event pairs
         torch.cuda.synchronize(dev)
@@ -392,6 +401,16 @@ def run_cuda(args, w):
         if dist is not None:
             dist.barrier()
         t_wall = t_wall1 - t_wall0
+    # the attention kernel alone (same inputs, same plan), for its roofline
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        g_pre.replay()
+        ev_att[i][0].record(stream)
+        g_att.replay()
+        ev_att[i][1].record(stream)
+        g_post.replay()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     att_ms = [a.elapsed_time(b) for a, b in ev_att]
     tot_ms = max_over_ranks(sum(step_ms), dist, dev)
@@ -494,7 +513,7 @@ def run_cuda(args, w):
 
     if rank == 0:
         peaks, peak_kind = load_peaks()
-        alg_bytes, flops, cache_bytes = algorithmic_counts(w)
+        alg_bytes, flops, cache_bytes = algorithmic_counts(w, args.lowp)
         att_avg_s = statistics.mean(att_ms) * 1e-3
         step_s = tot_ms * 1e-3 / args.steps
         tokens_per_step = w.B * w.Q
@@ -507,7 +526,7 @@ def run_cuda(args, w):
         achieved_gbs = alg_bytes / att_avg_s / 1e9
         achieved_tf = flops / att_avg_s / 1e12
         traffic = (kernel_traffic("decode_tc_full_width.md", "head_latent_attention_27_b300/csrc/decode_tc.cu")
-                   if w.name.startswith("full_width") else None)
+                   if w.name.startswith("full_width") and not args.lowp else None)
         if bound == "hbm":
             roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                     "frac": achieved_gbs / hbm, "traffic": traffic}
@@ -530,10 +549,12 @@ def run_cuda(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f16 (E4M3 cache)" if args.lowp else "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "S": int(w.lens[0]) if len(set(w.lens.tolist())) == 1 else
                        f"ragged, mean {float(np.mean(w.lens)):.0f}, max {int(np.max(w.lens))}", "H": w.H, "Q": w.Q,
-                       "d_c": w.d_c, "d_r": w.d_r, "page_size": 64, "n_split": n_split, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "d_c": w.d_c, "d_r": w.d_r, "page_size": 64, "n_split": n_split,
+                       "cache": ("low-precision rows: E4M3 latent + fp32 scale per 128 + bf16 RoPE key, 656 B/token"
+                                 if args.lowp else "bf16 rows, 1152 B/token"), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "l2": "flushed between steps (write > 2x L2 outside the per-step event pairs); "
                              f"cache {cache_bytes / 1e6:.0f} MB > L2"},
             "cache_read_gbs": cache_bytes / step_s / 1e9,
@@ -739,6 +760,8 @@ def main():
                     help="run N attention launches on one plan and exit (no timing; for ncu)")
     ap.add_argument("--absorb", action="store_true",
                     help="time the two absorption GEMMs at the full-width shape instead (own JSON line)")
+    ap.add_argument("--lowp", action="store_true",
+                    help="decode over the low-precision cache rows (E4M3 latent) instead of bf16 rows")
     ap.add_argument("--prefill", action="store_true",
                     help="time the expanded (prefill) form instead: projection + causal attention (own JSON line)")
     ap.add_argument("--prefill-tokens", type=int, default=4096)

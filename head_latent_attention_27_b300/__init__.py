@@ -232,9 +232,10 @@ def alloc_workspace(B: int, Q: int, H: int, d_c: int = 512, n_split: int = 0, de
 def _decode_args(cache: Cache, seq_lens, q_nope, q_rope, out, lse):
     torch = _torch()
     _need(seq_lens, "seq_lens", torch.int32, 1)
-    _need(q_nope, "q_nope", cache.data.dtype, 4)
-    _need(q_rope, "q_rope", cache.data.dtype, 4)
-    _need(out, "out", cache.data.dtype, 4)
+    qdt = torch.bfloat16 if cache.data.dtype == torch.uint8 else cache.data.dtype   # low-precision cache: bf16 q/out
+    _need(q_nope, "q_nope", qdt, 4)
+    _need(q_rope, "q_rope", qdt, 4)
+    _need(out, "out", qdt, 4)
     B, Q, H, dc = q_nope.shape
     if dc != cache.d_c or tuple(q_rope.shape) != (B, Q, H, cache.d_r) or tuple(out.shape) != (B, Q, H, cache.d_c):
         raise ValueError("q_nope/q_rope/out shapes do not match")

@@ -82,6 +82,20 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// 2-D tensor map of any element type: rows x cols elements, row stride in
+// bytes, box box_cols x box_rows.
+bool encode_2d_any(CUtensorMap* m, CUtensorMapDataType t, const void* base, uint64_t rows, uint64_t cols,
+                   uint64_t stride_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, t, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 tensor map over a row-major [d2][d1][d0] array, box
 // box0 x box1 x box2 (elements along d0 innermost).
 bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1,
@@ -224,14 +238,27 @@ mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShap
         a.scale = scale;
         return cuda_status(launch_decode_f32(a, P, ws, L, stream));
     }
-    if (c->dtype == MLA_FP8) return MLA_ERR_UNSUPPORTED;   // attention over the low-precision cache: not yet
     TcMaps maps;
     const uint64_t cache_rows = (uint64_t)c->num_pages * kTileTokens;
     const uint64_t qrows = (uint64_t)s.B * s.Q * s.H;
-    if (!encode_2d(&maps.kv_nope, c->data, cache_rows, 576, 576, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&maps.kv_rope, c->data, cache_rows, 576, 576, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !encode_2d(&maps.q_rope, q_rope, qrows, 64, 64, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
-        return MLA_ERR_CUDA;
+    const bool lowp = c->dtype == MLA_FP8;
+    if (lowp) {
+        // 656-byte rows: 512 E4M3 codes | 4 fp32 group scales | 64 bf16 RoPE values
+        constexpr uint64_t kRow = kFp8RowBytes;
+        if (!encode_2d_any(&maps.kv_nope, CU_TENSOR_MAP_DATA_TYPE_UINT8, c->data, cache_rows, kRow, kRow, 128, 64,
+                           CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_2d_any(&maps.kv_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c->data, cache_rows, kRow / 4, kRow, 4,
+                           64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_2d_any(&maps.kv_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->data, cache_rows, kRow / 2, kRow, 32,
+                           64, CU_TENSOR_MAP_SWIZZLE_64B))
+            return MLA_ERR_CUDA;
+    } else {
+        if (!encode_2d(&maps.kv_nope, c->data, cache_rows, 576, 576, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&maps.kv_rope, c->data, cache_rows, 576, 576, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+            return MLA_ERR_CUDA;
+        maps.kv_scale = maps.kv_rope;   // unused by the bf16 kernel
+    }
+    if (!encode_2d(&maps.q_rope, q_rope, qrows, 64, 64, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B)) return MLA_ERR_CUDA;
     TcArgs a;
     a.page_table = c->page_table;
     a.seq_lens = seq_lens;
@@ -247,7 +274,7 @@ mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShap
     a.cache = c->data;
     a.prefetch_tiles = kTcPrefetchTiles;
     a.total_rows = (int64_t)qrows;
-    return cuda_status(launch_decode_tc(maps, a, P, ws, L, stream));
+    return cuda_status(launch_decode_tc(maps, a, P, ws, L, stream, lowp));
 }
 
 mla_status_t do_combine(const mla_cache_t* c, DecodeShape s, void* out, float* lse, void* ws, size_t ws_bytes,

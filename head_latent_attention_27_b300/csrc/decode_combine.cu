@@ -15,6 +15,10 @@ constexpr int kWarpsPerBlock = 8;
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     combine_kernel(int32_t Q, int32_t H, int32_t d_c, int32_t out_bf16, void* __restrict__ out,
                    float* __restrict__ lse, void* ws, WsLayout L) {
+    // launched as a programmatic dependent of the attention kernel: its
+    // launch overlaps the attention's tail; every read of the partials waits
+    // here until that grid has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const WsView v = ws_view(ws, L);
     const int32_t u = blockIdx.x;
     if (u >= v.hdr->num_units) return;
@@ -118,9 +122,17 @@ cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t
     const int32_t U = B * units_per_seq(Q, H);
     if (U == 0) return cudaSuccess;
     const int32_t rows = min(kRowsPerUnit, Q * H);
-    dim3 grid(U, (rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
-    combine_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(Q, H, d_c, out_dtype == 0, out, lse, ws, L);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(U, (rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    cfg.blockDim = dim3(kWarpsPerBlock * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, Q, H, d_c, (int32_t)(out_dtype == 0), out, lse, ws, L);
 }
 
 }  // namespace mla

@@ -70,6 +70,20 @@ constexpr uint32_t QR_BYTES = BM * 64;
 constexpr uint32_t KN_BLK = BN * 128;                        // 64 dims x 64 tokens, 128B swizzle
 constexpr uint32_t KR_BYTES = BN * 64;                       // 32 dims x 64 tokens, 64B swizzle
 constexpr uint32_t STAGE_BYTES = 4 * KN_BLK + KR_BYTES;      // 36864
+// Low-precision rows: per tile and CTA the 256 latent codes of 64 tokens
+// are loaded as two 128-byte-wide boxes into the tile's latent boxes 2 and 3
+// and expanded in place to fp16 (boxes 0..3); the 4 fp32 group scales of
+// each token go to a small ring of their own.
+constexpr uint32_t LP_CODE_BOX = BN * 128;                   // 64 tokens x 128 codes
+constexpr uint32_t LP_SCALE_BYTES = BN * 16;                 // 64 tokens x 4 fp32
+constexpr uint32_t LP_STAGE_TX = 2 * LP_CODE_BOX + LP_SCALE_BYTES + KR_BYTES;
+// Byte offsets of a stage's boxes from the ring's base.
+__host__ __device__ constexpr uint32_t nope_box(uint32_t st, uint32_t kb) {   // 64 dims x 64 tokens
+    return st * STAGE_BYTES + kb * KN_BLK;
+}
+__host__ __device__ constexpr uint32_t rope_box(uint32_t st) {                 // 32 dims x 64 tokens
+    return st * STAGE_BYTES + 4 * KN_BLK;
+}
 constexpr uint32_t OFF_KV = OFF_QR + QR_BYTES;
 constexpr uint32_t P_BYTES = BM * BN * 2;                    // bf16 P, 128 rows x 128 B, 128B swizzle
 constexpr uint32_t OFF_P = OFF_KV + NSTAGE * STAGE_BYTES;
@@ -79,7 +93,8 @@ constexpr uint32_t OFF_BAR = OFF_X + 2 * X_BYTES;
 constexpr uint32_t BAR_BYTES = 512;
 constexpr uint32_t OFF_M = OFF_BAR + BAR_BYTES;                // [2 slots][128 rows] fp32 running max
 constexpr uint32_t OFF_LM = OFF_M + 2 * BM * 4;                // [2][128] float2 (row sum, its max)
-constexpr uint32_t SMEM_USED = OFF_LM + 2 * BM * 8;
+constexpr uint32_t OFF_SC = OFF_LM + 2 * BM * 8;                // [NSTAGE] low-precision group scales
+constexpr uint32_t SMEM_USED = OFF_SC + NSTAGE * LP_SCALE_BYTES;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;            // + alignment slack
 
 static_assert(OFF_KV % 1024 == 0 && STAGE_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_X % 1024 == 0,
@@ -105,7 +120,8 @@ enum : int {
     B_LFULL = B_MREADY + 2,         // [2] a group's row sum of a piece published (piece parity)
     B_LFREE = B_LFULL + 2,          // [2] ... and read
     B_OFREE = B_LFREE + 2,          // epilogue has read O; the next piece may overwrite it
-    NUM_BARS
+    B_LPFULL,                       // [NSTAGE] low-precision tile landed (codes, scales, RoPE)
+    NUM_BARS = B_LPFULL + NSTAGE
 };
 static_assert(NUM_BARS * 8 <= BAR_BYTES - 16, "barrier area");
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + BAR_BYTES - 16;
@@ -116,6 +132,10 @@ constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384, TM_COLS = 512;
 
 constexpr uint32_t IDESC_QK = idesc_bf16(128, BN, 0, 0);   // S[128x64] = Q . K^T, K-major operands
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, 0, 1);  // O[128x256] += P . V, V MN-major
+// Low-precision cache: the latent operands (q_nope, the dequantised cache
+// tile, P) are fp16; the RoPE part stays bf16 (its MMAs keep IDESC_QK/QK2).
+constexpr uint32_t IDESC_QK_H = idesc_f16(128, BN, 0, 0);
+constexpr uint32_t IDESC_PV_H = idesc_f16(128, 256, 0, 1);
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -124,6 +144,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi);
+// bf16 pair -> fp16 pair (each value rounded to nearest fp16).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
+    return pack_f16x2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+template <bool kHalf>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi);
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack_p<false>(float lo, float hi) { return pack_bf16x2(lo, hi); }
+template <>
+__device__ __forceinline__ uint32_t pack_p<true>(float lo, float hi) { return pack_f16x2(lo, hi); }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     const __half2 v = __floats2half2_rn(lo, hi);
@@ -217,9 +251,71 @@ struct TileCursor {
     }
 };
 
+// Dequantise one tile's low-precision latent codes in place (producer warp,
+// all 32 lanes): codes of latent dims [0,128) of this CTA's half sit in box
+// 2, dims [128,256) in box 3 ([64 tokens][128 codes], unswizzled); value =
+// E4M3(code) * group scale, written as fp16 into boxes 0..3 in the 128-byte
+// swizzled K-major layout the MMAs read.  The first half goes to boxes 0
+// and 1 (no overlap with any code); the second half's codes are all read
+// into registers before its outputs overwrite boxes 2 and 3.
+__device__ __forceinline__ void expand16(uint8_t* ring, uint32_t st, uint32_t box0, int row, int c8, uint4 cw,
+                                         float sc) {
+    const __half2 s2 = __float2half2_rn(sc);
+    uint32_t w[8];
+    const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t lo, hi;
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(lo), "=r"(hi) : "r"(cws[j]));
+        const __half2 l2 = __hmul2(*reinterpret_cast<const __half2*>(&lo), s2);
+        const __half2 h2 = __hmul2(*reinterpret_cast<const __half2*>(&hi), s2);
+        w[2 * j] = *reinterpret_cast<const uint32_t*>(&l2);
+        w[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    // dims 16*c8 .. +16 of the half -> box box0 + (c8 >> 2), 16-byte chunks 2*(c8&3), +1
+    uint8_t* rowp = ring + nope_box(st, box0 + (c8 >> 2)) + row * 128;
+    const int ch = 2 * (c8 & 3), sw = row & 7;
+    *reinterpret_cast<uint4*>(rowp + ((ch ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ sw) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__device__ __forceinline__ void dequant_tile(uint8_t* ring, uint32_t st, const float* scales, uint32_t rank,
+                                             int lane) {
+    // All 16 chunks of codes (and their scales) of a half are loaded before
+    // any is expanded: the loads then overlap instead of each one waiting
+    // behind the previous chunk's stores (the compiler cannot reorder shared
+    // loads above possibly aliasing shared stores).  The second half's codes
+    // sit in box 3, which its outputs overwrite: all lanes have read them
+    // (__syncwarp) before the first store.
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        const uint8_t* codes = ring + nope_box(st, 2 + half);
+        uint4 cw[16];
+        float sc[16];
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+            const int pidx = it * 32 + lane;           // 512 chunks of 16 codes per half
+            const int row = pidx >> 3;
+            cw[it] = *reinterpret_cast<const uint4*>(codes + row * 128 + (pidx & 7) * 16);
+            sc[it] = scales[row * 4 + 2 * rank + half];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+            const int pidx = it * 32 + lane;
+            expand16(ring, st, 2 * half, pidx >> 3, pidx & 7, cw[it], sc[it]);
+        }
+    }
+    __syncwarp();
+}
+
+template <bool kLowp>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv_nope, const __grid_constant__ CUtensorMap tm_kv_rope,
-                     const __grid_constant__ CUtensorMap tm_q_rope, const TcArgs a, void* ws, const WsLayout L) {
+                     const __grid_constant__ CUtensorMap tm_q_rope, const __grid_constant__ CUtensorMap tm_kv_scale,
+                     const TcArgs a, void* ws, const WsLayout L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
@@ -242,6 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(bar(B_KVFULL + s), 1);
             mbar_init(bar(B_KVEMPTY + s), 1);
+            mbar_init(bar(B_LPFULL + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_SFULL + s), 1);
@@ -268,6 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_kv_nope);
         tma_prefetch_desc(&tm_kv_rope);
         tma_prefetch_desc(&tm_q_rope);
+        if constexpr (kLowp) tma_prefetch_desc(&tm_kv_scale);
     }
     tc_fence_before();
     __syncthreads();
@@ -281,7 +379,97 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int32_t RB = units_per_seq(a.Q, a.H);
     const int32_t max_tokens = a.max_pages_per_seq * kTileTokens;
 
-    if (warp == 0) {
+    if (warp == 0 && kLowp) {
+        // -------------------------------- TMA producer + in-place dequantiser
+        // One loop, never blocking on one condition while the other could
+        // progress: lane 0 issues the loads of the next tile as soon as its
+        // stage is free (and, at a piece's first tile, the previous piece has
+        // released q_rope); the whole warp expands the oldest landed tile and
+        // marks it full for the MMAs.  Gives up (timeout status) after the
+        // same time limit as every other wait when neither can progress.
+        const uint64_t pol = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
+        uint8_t* ring = smem + OFF_KV;
+        uint32_t q_cnt = 0, issued = 0, expanded = 0, total = 0;
+        for (int32_t p = p_begin; p < p_end; ++p) total += (uint32_t)(v.pieces[p].t_end - v.pieces[p].t_begin);
+        TileCursor ic;
+        ic.init(v.pieces, p_begin, p_end);
+        bool ok = true;
+        uint64_t idle_since = 0;
+        while (ok && expanded < total) {
+            bool progressed = false;
+            // 1. loads of tile `issued`
+            if (issued < total) {
+                const uint32_t st = issued % NSTAGE, ph = (issued / NSTAGE) & 1u;
+                int go = 0;
+                if (lane == 0) {
+                    const bool new_piece = ic.first();
+                    go = mbar_try_wait(bar(B_KVEMPTY + st), ph ^ 1u) &&
+                         (!new_piece || mbar_try_wait(bar(B_QREMPTY), (q_cnt & 1u) ^ 1u));
+                    if (go) {
+                        const int32_t b = ic.pc.unit / RB, rb = ic.pc.unit % RB;
+                        if (new_piece) {
+                            mbar_arrive_expect_tx(bar(B_QRFULL), QR_BYTES);
+                            tma_load_2d(sbase + OFF_QR, &tm_q_rope, bar(B_QRFULL), 32 * rank, b * QH + rb * BM, pol);
+                            ++q_cnt;
+                        }
+                        int32_t page = a.page_table[(int64_t)b * a.max_pages_per_seq + ic.t];
+                        if (page < 0 || page >= a.num_pages) {
+                            atomicCAS(status, 0, 1);
+                            page = 0;
+                        }
+                        const uint32_t fb = bar(B_LPFULL + st);
+                        mbar_arrive_expect_tx(fb, LP_STAGE_TX);
+                        const int32_t y0 = page * BN;
+                        tma_load_2d(sbase + OFF_KV + nope_box(st, 2), &tm_kv_nope, fb, 256 * rank, y0, pol);
+                        tma_load_2d(sbase + OFF_KV + nope_box(st, 3), &tm_kv_nope, fb, 256 * rank + 128, y0, pol);
+                        tma_load_2d(sbase + OFF_SC + st * LP_SCALE_BYTES, &tm_kv_scale, fb, 128, y0, pol);
+                        tma_load_2d(sbase + OFF_KV + rope_box(st), &tm_kv_rope, fb, 264 + 32 * rank, y0, pol);
+                        ic.next();
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, go, 0)) {
+                    ++issued;
+                    progressed = true;
+                }
+            }
+            // 2. expand tile `expanded` once it has landed
+            if (expanded < issued) {
+                const uint32_t st = expanded % NSTAGE, ph = (expanded / NSTAGE) & 1u;
+                const int landed = lane == 0 ? (mbar_try_wait(bar(B_LPFULL + st), ph) ? 1 : 0) : 0;
+                if (__shfl_sync(0xffffffffu, landed, 0)) {
+                    dequant_tile(ring, st, reinterpret_cast<const float*>(smem + OFF_SC + st * LP_SCALE_BYTES),
+                                 rank, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_KVFULL + st));
+                    ++expanded;
+                    progressed = true;
+                }
+            }
+            if (progressed) {
+                idle_since = 0;
+            } else {
+                __nanosleep(32);   // poll gently: this warp shares its scheduler with softmax warps
+                const uint64_t now = global_timer_ns();
+                if (idle_since == 0) idle_since = now;
+                int stop = 0;
+                if (lane == 0 && (*abort_flag || now - idle_since > kWaitLimitNs)) {
+                    if (!*abort_flag) {
+                        *abort_flag = 1;
+                        atomicExch(status, 4 /* MLA_ERR_TIMEOUT */);
+                    }
+                    stop = 1;
+                }
+                if (__shfl_sync(0xffffffffu, stop, 0)) ok = false;
+            }
+        }
+        if (lane == 0) {
+            // drain this CTA's copies still in flight (abort path)
+            for (uint32_t i = expanded; i < issued; ++i)
+                drain_wait(bar(B_LPFULL + i % NSTAGE), (i / NSTAGE) & 1u);
+            if (q_cnt > 0) drain_wait(bar(B_QRFULL), (q_cnt - 1) & 1u);
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
@@ -323,12 +511,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     const uint32_t fb = bar(B_KVFULL + stage);
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    const uint32_t dst = sbase + OFF_KV + stage * STAGE_BYTES;
+                    const uint32_t ring = sbase + OFF_KV;
                     const int32_t y0 = page * BN;
 #pragma unroll
                     for (int kb = 0; kb < 4; ++kb)
-                        tma_load_2d(dst + kb * KN_BLK, &tm_kv_nope, fb, 256 * rank + 64 * kb, y0, pol);
-                    tma_load_2d(dst + 4 * KN_BLK, &tm_kv_rope, fb, 512 + 32 * rank, y0, pol);
+                        tma_load_2d(ring + nope_box(stage, kb), &tm_kv_nope, fb, 256 * rank + 64 * kb, y0, pol);
+                    tma_load_2d(ring + rope_box(stage), &tm_kv_rope, fb, 512 + 32 * rank, y0, pol);
                     issued_mask |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == NSTAGE) {
@@ -375,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk)   // 256 latent dims, A = q_nope from TMEM
                     umma_ts(tS, tQ + kk * 8, bn0 + (uint64_t)((((kk >> 2) * KN_BLK + (kk & 3) * 32)) >> 4),
-                            IDESC_QK, kk != 0 ? 1u : 0u);
+                            kLowp ? IDESC_QK_H : IDESC_QK, kk != 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)    // 32 RoPE dims, A = q_rope from smem
                     umma_ss(tS, adesc_rope + (uint64_t)(kk * 2), br0 + (uint64_t)(kk * 2), IDESC_QK, 1u);
@@ -416,7 +604,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool first = pv.first();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)   // descriptors: start address + offset / 16
-                    umma_ss(tO, ap0 + (uint64_t)(kk * 2), bv0 + (uint64_t)(kk * 128), IDESC_PV,
+                    umma_ss(tO, ap0 + (uint64_t)(kk * 2), bv0 + (uint64_t)(kk * 128), kLowp ? IDESC_PV_H : IDESC_PV,
                             (first && kk == 0) ? 0u : 1u);
                 umma_commit(bar(B_PVDONE + slot));
                 umma_commit(bar(B_KVEMPTY + pv_stage));
@@ -470,6 +658,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint4 y = have ? src[c0 / 4 + 4 + i] : make_uint4(0, 0, 0, 0);
                     r0[4 * i] = x.x; r0[4 * i + 1] = x.y; r0[4 * i + 2] = x.z; r0[4 * i + 3] = x.w;
                     r1[4 * i] = y.x; r1[4 * i + 1] = y.y; r1[4 * i + 2] = y.z; r1[4 * i + 3] = y.w;
+                }
+                if constexpr (kLowp) {   // the latent MMAs of the low-precision cache take fp16 queries
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        r0[i] = bf16x2_to_f16x2(r0[i]);
+                        r1[i] = bf16x2_to_f16x2(r1[i]);
+                    }
                 }
                 tmem_st16(tQ + c0, r0);
                 tmem_st16(tQ + c0 + 16, r1);
@@ -605,7 +800,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const float p0 = fast_exp2(x.x);   // exp2(-inf) = 0
                         const float p1 = fast_exp2(x.y);
                         add2_to(ls[2 * (i & 1)], ls[2 * (i & 1) + 1], p0, p1);
-                        w[i] = pack_bf16x2(p0, p1);
+                        w[i] = pack_p<kLowp>(p0, p1);
                     }
                     *reinterpret_cast<uint4*>(prow + ((c ^ rsw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
@@ -639,13 +834,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (tok0 + BN > vis_hi) {
                 const int32_t nvalid = max(0, vis_hi - tok0);
                 const int32_t nrows = BN - nvalid;
-                uint8_t* st_base = smem + OFF_KV + ((g % NSTAGE) * STAGE_BYTES);
+                const uint32_t st = g % NSTAGE;
                 const int32_t chunks = nrows * 8 * 4;
                 for (int32_t i = gtid; i < chunks; i += 128) {
                     const int32_t kb = i / (nrows * 8);
                     const int32_t rem = i % (nrows * 8);
                     const int32_t rr = nvalid + rem / 8, cc = rem % 8;
-                    *reinterpret_cast<uint4*>(st_base + kb * KN_BLK + rr * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(smem + OFF_KV + nope_box(st, kb) + rr * 128 + cc * 16) =
+                        make_uint4(0, 0, 0, 0);
                 }
             }
             // 8. publish P(g)
@@ -771,6 +967,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ teardown
+    // this CTA's work is done: the dependent combine grid may be scheduled
+    // (it waits for this grid's completion before reading anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // the peer no longer writes into this CTA's smem
@@ -785,7 +984,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 size_t decode_tc_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t decode_tc_max_clusters(int32_t* clusters) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
@@ -799,16 +1001,20 @@ cudaError_t decode_tc_max_clusters(int32_t* clusters) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<false>, &cfg);
     if (e != cudaSuccess) return e;
     *clusters = n;
     return cudaSuccess;
 }
 
 cudaError_t launch_decode_tc(const TcMaps& maps, const TcArgs& a, int32_t num_clusters, void* ws,
-                             const WsLayout& L, cudaStream_t stream) {
-    decode_tc_kernel<<<2 * num_clusters, kThreads, SMEM_BYTES, stream>>>(maps.kv_nope, maps.kv_rope, maps.q_rope,
-                                                                         a, ws, L);
+                             const WsLayout& L, cudaStream_t stream, bool lowp) {
+    if (lowp)
+        decode_tc_kernel<true><<<2 * num_clusters, kThreads, SMEM_BYTES, stream>>>(
+            maps.kv_nope, maps.kv_rope, maps.q_rope, maps.kv_scale, a, ws, L);
+    else
+        decode_tc_kernel<false><<<2 * num_clusters, kThreads, SMEM_BYTES, stream>>>(
+            maps.kv_nope, maps.kv_rope, maps.q_rope, maps.kv_scale, a, ws, L);
     return cudaGetLastError();
 }
 

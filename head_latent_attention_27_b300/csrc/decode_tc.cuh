@@ -26,9 +26,11 @@ struct TcArgs {
 };
 
 struct TcMaps {
-    CUtensorMap kv_nope;  // cache [pages*64][576], box 64 x 64, 128-byte swizzle
-    CUtensorMap kv_rope;  // same tensor, box 32 x 64, 64-byte swizzle
-    CUtensorMap q_rope;   // [B*Q*H][64], box 32 x 128, 64-byte swizzle
+    CUtensorMap kv_nope;   // bf16 cache [pages*64][576], box 64 x 64, 128-byte swizzle;
+                           // low-precision cache: the rows as bytes [pages*64][656], box 128 x 64
+    CUtensorMap kv_rope;   // bf16 RoPE keys, box 32 x 64, 64-byte swizzle (bf16 view of either row format)
+    CUtensorMap q_rope;    // [B*Q*H][64], box 32 x 128, 64-byte swizzle
+    CUtensorMap kv_scale;  // low-precision cache only: fp32 view [pages*64][164], box 4 x 64 (group scales)
 };
 
 // Dynamic shared memory of the kernel (bytes) and its cluster size.
@@ -46,7 +48,9 @@ constexpr int kTcPrefetchTiles = MLA_TC_PREFETCH_TILES;
 // Maximum number of co-resident 2-CTA clusters on the current device.
 cudaError_t decode_tc_max_clusters(int32_t* clusters);
 
+// lowp: the cache holds low-precision rows (E4M3 latent + fp32 group scales +
+// bf16 RoPE key, 656 bytes); otherwise bf16 rows.
 cudaError_t launch_decode_tc(const TcMaps& maps, const TcArgs& a, int32_t num_clusters, void* ws,
-                             const WsLayout& L, cudaStream_t stream);
+                             const WsLayout& L, cudaStream_t stream, bool lowp);
 
 }  // namespace mla

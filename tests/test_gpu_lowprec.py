@@ -12,7 +12,7 @@ import torch
 
 import oracle as O
 import synth
-from gpu_util import build_cache, mla_pkg
+from gpu_util import build_cache, compare, mla_pkg
 from oracle import lowprec_cache as LP
 from synth.device import upload
 
@@ -49,3 +49,60 @@ def test_quantising_append_stores_the_quantised_bf16_row():
     # the dequantised latent is within the E4M3 bound of the bf16 row
     deq = LP.dequantize_latent(codes, scales)
     assert np.all(np.abs(deq - rows[:, :512]) <= 2.0 ** -4 * np.abs(rows[:, :512]) + scales.repeat(128, axis=1) * 2.0 ** -10)
+
+
+# --------------------------------------------------- decode over the rows --
+
+def _oracle_lowp(w, b):
+    """Oracle decode of sequence b over the oracle's own low-precision cache:
+    its bf16 rows, quantised and dequantised by the oracle."""
+    C, R = O.sequence_cache(w, b)
+    codes, scales, _ = LP.quantize_cache_rows(np.concatenate([C, R], axis=1), 512)
+    return O.decode_sequence(w, b, cache=(LP.dequantize_latent(codes, scales), R))
+
+
+def _run_lowp(w, n_split=0):
+    mla = mla_pkg()
+    cache8, d = _fp8_cache(w)
+    out = torch.full((w.B, w.Q, w.H, w.d_c), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.B, w.Q, w.H), float("nan"), dtype=torch.float32, device="cuda")
+    ws = mla.alloc_workspace(w.B, w.Q, w.H, w.d_c, n_split, "cuda")
+    scale = 1.0 / np.sqrt(w.d_h + w.d_r)
+    if n_split:
+        mla.mla_decode_split_combine(cache8, d["seq_lens"], d["q_nope"], d["q_rope"], out, n_split, lse=lse,
+                                     workspace=ws, softmax_scale=scale)
+    else:
+        mla.mla_decode(cache8, d["seq_lens"], d["q_nope"], d["q_rope"], out, lse=lse, workspace=ws,
+                       softmax_scale=scale)
+    status = mla.mla_decode_read_status(ws)
+    assert status == mla.MLA_OK, mla.mla_status_string(status)
+    return out.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+LOWP_CASES = [
+    # name, lens, H, Q, q_gain, n_split
+    ("lp_h128_ragged", [1, 2, 63, 64, 65, 127, 128, 129, 300, 1000], 128, 1, 1.0, 0),
+    ("lp_h128_q2", [1, 2, 64, 65, 500, 3001], 128, 2, 1.0, 0),
+    ("lp_h16", [1, 5, 64, 65, 200, 777], 16, 1, 1.0, 0),
+    ("lp_sharp", [50, 700, 2049], 128, 1, 16.0, 0),
+    ("lp_split", [1, 65, 640, 1999, 4096], 128, 1, 1.0, 32),
+]
+
+
+@pytest.mark.parametrize("case", LOWP_CASES, ids=[c[0] for c in LOWP_CASES])
+def test_decode_over_the_low_precision_cache(case):
+    name, lens, H, Q, q_gain, n_split = case
+    w = synth.custom_bf16(name, 1500 + len(name), lens, H=H, Q=Q, paged=True, q_gain=q_gain)
+    out, lse = _run_lowp(w, n_split)
+    ref = [_oracle_lowp(w, b) for b in range(w.B)]
+    compare(w, out, lse, ref=(np.stack([r[0] for r in ref]), np.stack([r[1] for r in ref])))
+
+
+def test_decode_over_the_low_precision_cache_full_width():
+    """The full-width workload (B=64, S=4096, H=128) over the low-precision
+    cache, every sequence against the oracle."""
+    w = synth.full_width()
+    out, lse = _run_lowp(w)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    ref = [_oracle_lowp(w, b) for b in range(w.B)]
+    compare(w, out, lse, ref=(np.stack([r[0] for r in ref]), np.stack([r[1] for r in ref])))
