@@ -511,6 +511,31 @@ def run_cuda(args, w):
             torch.equal(h_lse[(args.steps - 1) % n_sets], lse.cpu())):
         raise RuntimeError("e2e result differs from the device-resident step")
 
+    # the host link alone: the same copies with no compute, each direction
+    # alone and both together, so that the e2e rate can be read against it
+    def copies_ms(h2d_on: bool, d2h_on: bool) -> float:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(s_in)
+        s_out.wait_stream(s_in)
+        for step in range(args.steps):
+            i = step % n_sets
+            if h2d_on:
+                with torch.cuda.stream(s_in):
+                    for t, h in ((d_qn[i], h_qn), (d_qr[i], h_qr), (d_c[i], h_c), (d_k[i], h_k)):
+                        t.copy_(h, non_blocking=True)
+            if d2h_on:
+                with torch.cuda.stream(s_out):
+                    h_out[i].copy_(d_out[i], non_blocking=True)
+                    h_lse[i].copy_(d_lse[i], non_blocking=True)
+        s_in.wait_stream(s_out)
+        b.record(s_in)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / args.steps
+
+    copies_ms(True, True)   # warm
+    link_h2d, link_d2h, link_both = copies_ms(True, False), copies_ms(False, True), copies_ms(True, True)
+
     if rank == 0:
         peaks, peak_kind = load_peaks()
         alg_bytes, flops, cache_bytes = algorithmic_counts(w, args.lowp)
@@ -525,8 +550,9 @@ def run_cuda(args, w):
         bound = "hbm" if t_mem >= t_tc else "tensor"
         achieved_gbs = alg_bytes / att_avg_s / 1e9
         achieved_tf = flops / att_avg_s / 1e12
-        traffic = (kernel_traffic("decode_tc_full_width.md", "head_latent_attention_27_b300/csrc/decode_tc.cu")
-                   if w.name.startswith("full_width") and not args.lowp else None)
+        traffic = (kernel_traffic("decode_tc_lowp_full_width.md" if args.lowp else "decode_tc_full_width.md",
+                                  "head_latent_attention_27_b300/csrc/decode_tc.cu")
+                   if w.name.startswith("full_width") else None)
         if bound == "hbm":
             roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                     "frac": achieved_gbs / hbm, "traffic": traffic}
@@ -566,7 +592,9 @@ def run_cuda(args, w):
                                        f"{cpu_steps} pass(es) in {cpu_el:.1f} s"},
             "e2e": {"value": whole_job_rate(world, tokens_per_step, args.steps, e2e_tot), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i (two buffer sets)"},
+                    "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i (two buffer sets)",
+                    "copies_only_ms_per_step": {"h2d": link_h2d, "d2h": link_d2h, "both": link_both},
+                    "link_gbs": {"h2d": h2d / link_h2d / 1e6, "d2h": d2h / link_d2h / 1e6}},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
@@ -577,8 +605,9 @@ def run_cuda(args, w):
         dist.destroy_process_group()
 
 
-def run_profile_attend(w, n: int) -> None:
-    """The attention kernel alone, `n` launches on one plan, for profilers."""
+def run_profile_attend(w, n: int, lowp: bool = False) -> None:
+    """The attention kernel alone, `n` launches on one plan, for profilers
+    (`lowp`: over the low-precision cache rows)."""
     import torch
 
     import head_latent_attention_27_b300 as mla
@@ -587,7 +616,10 @@ def run_profile_attend(w, n: int) -> None:
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     d = upload(w, dev)
-    pool = empty_pool(w, dev, fill_nan=False)
+    if lowp:
+        pool = torch.zeros((w.num_pages, 64, mla.FP8_ROW_BYTES), dtype=torch.uint8, device=dev)
+    else:
+        pool = empty_pool(w, dev, fill_nan=False)
     cache = mla.Cache(pool, d["page_table"], w.d_c, w.d_r)
     mla.mla_cache_append(cache, d["raw_c"], d["raw_k"], d["seq_ids"], d["positions"], eps=w.eps,
                          rope_base=w.rope_base, flags=mla.MLA_APPEND_RMSNORM | mla.MLA_APPEND_ROPE)
@@ -740,7 +772,10 @@ def run_prefill_bench(args) -> None:
                     "tflops": f_proj / (proj_ms * 1e-3) / 1e12, "frac": f_proj / (proj_ms * 1e-3) / 1e12 / tc},
         "roofline": {"bound": "tensor", "kernel": "prefill_attn_kernel", "achieved": f_attn / (attn_ms * 1e-3) / 1e12,
                      "peak": tc, "unit": "TFLOP/s", "frac": f_attn / (attn_ms * 1e-3) / 1e12 / tc,
-                     "kernel_ms": attn_ms, "alg_flops": f_attn, "peak_source": f"{src} burst", "traffic": None},
+                     "kernel_ms": attn_ms, "alg_flops": f_attn, "peak_source": f"{src} burst",
+                     "traffic": (kernel_traffic("prefill_attn_T4096_H128.md",
+                                                "head_latent_attention_27_b300/csrc/prefill.cu")
+                                 if T == 4096 and H == 128 else None)},
         "clocks": clk.summary(t0, t1),
     }
     print(json.dumps(line), flush=True)
@@ -780,7 +815,7 @@ def main():
     if args.n_split is None:
         args.n_split = 64 if args.workload == "long_split" else 0
     if args.profile_attend > 0:
-        run_profile_attend(w, args.profile_attend)
+        run_profile_attend(w, args.profile_attend, args.lowp)
         return
     if args.impl == "reference":
         run_reference(args, w)
