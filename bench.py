@@ -559,7 +559,8 @@ def run_cuda(args, w):
         else:
             roof = {"bound": "tensor", "achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s",
                     "frac": achieved_tf / tc_peak, "traffic": traffic}
-        roof.update({"kernel": "decode_tc_kernel (mla_decode_attend)", "peak_source": f"{peak_kind} burst",
+        roof.update({"kernel": ("decode_sh_kernel" if w.Q * w.H <= 16 and not args.lowp else "decode_tc_kernel")
+                               + " (mla_decode_attend)", "peak_source": f"{peak_kind} burst",
                      "kernel_ms": att_avg_s * 1e3, "alg_bytes": alg_bytes, "alg_flops": flops,
                      "roofline_ms": max(t_mem, t_tc) * 1e3, "frac_of_roofline": max(t_mem, t_tc) / att_avg_s,
                      "tensor_frac": achieved_tf / tc_peak})

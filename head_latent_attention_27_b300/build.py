@@ -19,7 +19,7 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla.so")
 
 SOURCES = ["api.cu", "absorb.cu", "append.cu", "decode_plan.cu", "decode_combine.cu", "decode_f32.cu",
-           "decode_tc.cu", "noalloc.cu", "prefill.cu"]
+           "decode_sh.cu", "decode_tc.cu", "noalloc.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -11,6 +11,7 @@
 #include "append.cuh"
 #include "decode_f32.cuh"
 #include "decode_plan.cuh"
+#include "decode_sh.cuh"
 #include "decode_tc.cuh"
 #include "prefill.cuh"
 #include "mla.h"
@@ -163,13 +164,21 @@ mla_status_t check_cache(const mla_cache_t* c) {
     return MLA_OK;
 }
 
-int32_t num_workers(const DeviceInfo* d, int32_t dtype) {
-    return dtype == MLA_FP32 ? d->sms : d->tc_clusters;
-}
-
 struct DecodeShape {
     int32_t B, Q, H, n_split;
 };
+
+// bf16 units of at most 16 query rows go to the single-SM kernel
+// (decode_sh.cu); larger units to the two-SM tensor-memory kernel.
+bool small_rows(const mla_cache_t* c, DecodeShape s) {
+    return c->dtype == MLA_BF16 && (int64_t)s.Q * s.H <= kShMaxRows;
+}
+
+// Workers of the plan: one CTA per SM on the fp32 and small-unit paths, one
+// 2-CTA cluster on the tensor-memory path.
+int32_t num_workers(const DeviceInfo* d, const mla_cache_t* c, DecodeShape s) {
+    return (c->dtype == MLA_FP32 || small_rows(c, s)) ? d->sms : d->tc_clusters;
+}
 
 mla_status_t check_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeShape s, const void* q_nope,
                           const void* q_rope, const void* out) {
@@ -201,7 +210,7 @@ mla_status_t do_plan(const mla_cache_t* c, const int32_t* seq_lens, DecodeShape 
                      cudaStream_t stream) {
     const DeviceInfo* d = device_info();
     if (!d || d->err != cudaSuccess || d->sms <= 0) return MLA_ERR_CUDA;
-    const int32_t P = num_workers(d, c->dtype);
+    const int32_t P = num_workers(d, c, s);
     if (P <= 0) return MLA_ERR_CUDA;
     const WsLayout L = ws_layout(s.B, s.Q, s.H, c->d_c, s.n_split, P);
     mla_status_t st = check_workspace(ws, ws_bytes, L);
@@ -215,7 +224,7 @@ mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShap
                        cudaStream_t stream) {
     const DeviceInfo* d = device_info();
     if (!d || d->err != cudaSuccess || d->sms <= 0) return MLA_ERR_CUDA;
-    const int32_t P = num_workers(d, c->dtype);
+    const int32_t P = num_workers(d, c, s);
     const WsLayout L = ws_layout(s.B, s.Q, s.H, c->d_c, s.n_split, P);
     mla_status_t st = check_workspace(ws, ws_bytes, L);
     if (st != MLA_OK) return st;
@@ -238,8 +247,25 @@ mla_status_t do_attend(const mla_cache_t* c, const int32_t* seq_lens, DecodeShap
         a.scale = scale;
         return cuda_status(launch_decode_f32(a, P, ws, L, stream));
     }
-    TcMaps maps;
     const uint64_t cache_rows = (uint64_t)c->num_pages * kTileTokens;
+    if (small_rows(c, s)) {
+        CUtensorMap kv;
+        if (!encode_2d(&kv, c->data, cache_rows, 576, 576, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
+        ShArgs a;
+        a.page_table = c->page_table;
+        a.seq_lens = seq_lens;
+        a.q_nope = q_nope;
+        a.q_rope = q_rope;
+        a.out = out;
+        a.lse = lse;
+        a.num_pages = c->num_pages;
+        a.max_pages_per_seq = c->max_pages_per_seq;
+        a.Q = s.Q;
+        a.H = s.H;
+        a.scale_log2 = scale * 1.4426950408889634f;
+        return cuda_status(launch_decode_sh(kv, a, P, ws, L, stream));
+    }
+    TcMaps maps;
     const uint64_t qrows = (uint64_t)s.B * s.Q * s.H;
     const bool lowp = c->dtype == MLA_FP8;
     if (lowp) {
@@ -281,7 +307,7 @@ mla_status_t do_combine(const mla_cache_t* c, DecodeShape s, void* out, float* l
                         cudaStream_t stream) {
     const DeviceInfo* d = device_info();
     if (!d || d->err != cudaSuccess || d->sms <= 0) return MLA_ERR_CUDA;
-    const int32_t P = num_workers(d, c->dtype);
+    const int32_t P = num_workers(d, c, s);
     const WsLayout L = ws_layout(s.B, s.Q, s.H, c->d_c, s.n_split, P);
     mla_status_t st = check_workspace(ws, ws_bytes, L);
     if (st != MLA_OK) return st;
