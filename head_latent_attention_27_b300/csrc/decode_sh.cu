@@ -9,7 +9,7 @@
 //     O   [16 x 512] += P [16 x 32] . V [32 x 512]    (m16n8k16 bf16 MMAs)
 // where K = [c || k^R] and V = c are the same cached rows.
 //
-// Warps (288 threads):
+// Warps (384 threads, three warpgroups):
 //   warps 0-3, 4-7  two consumer groups taking alternate stages; each has
 //                   its own running max / sum / O and the two are merged
 //                   at the end of a piece (flash-decoding merge inside the
@@ -24,7 +24,8 @@
 //                       accumulator layout of two adjacent 8-token score
 //                       tiles is the A layout of one 16-token k-step);
 //                     - accumulates O for dims [128w, 128w + 128).
-//   warp 8          TMA producer (one lane).
+//   warp 8          TMA producer (one lane); warps 9-11 idle (they only
+//                   give their registers to the consumers).
 // Every wait is bounded (ptx.cuh: bounded_wait): on a timeout the kernel
 // records MLA_ERR_TIMEOUT, waits (time-limited) for its own copies in
 // flight and exits.
@@ -42,8 +43,18 @@ constexpr int ST = 32;                // tokens per stage
 constexpr int NSTAGE = 4;
 constexpr int kGroups = 2;
 constexpr int kGroupWarps = 4;
-constexpr int kProducerWarp = kGroups * kGroupWarps;   // warp 8
-constexpr int kThreads = 32 * (kProducerWarp + 1);     // 288
+constexpr int kProducerWarp = kGroups * kGroupWarps;   // warp 8, first of the producer warpgroup
+constexpr int kThreads = 32 * (kProducerWarp + 4);     // 384: three warpgroups
+// Register split (setmaxnreg): the launch gives every thread the same
+// count; the producer warpgroup (one busy lane) hands most of its share to
+// the two consumer warpgroups, whose query fragments, scores and O tile
+// would not fit the 168 registers of a three-warpgroup launch.  The shares
+// add up to the launch's total of 384 x 168; the launcher checks the
+// compiled count before every launch.
+constexpr int kProducerRegs = 24;
+constexpr int kConsumerRegs = 240;
+constexpr int kLaunchRegs = 168;
+static_assert(4 * kProducerRegs + 8 * kConsumerRegs <= 12 * kLaunchRegs, "register split within the launch");
 constexpr int kBoxes = 9;                               // 8 latent boxes + the RoPE box
 constexpr int kQkDims = 576 / kGroupWarps;              // 144 dims scored per warp
 constexpr int kQkSteps = kQkDims / 16;                  // 9 k-steps
@@ -76,11 +87,36 @@ static_assert(SMEM_BYTES <= 232448, "fits in 227 KB");
 static_assert(kQkDims % 16 == 0 && (512 % kQkDims) % 16 == 0, "a k-step never straddles latent and RoPE dims");
 
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: O and l are rescaled only when the max grows by > 2^8
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// (x, y) += (a, b) and (x*a + c, y*b + d) as packed f32x2 operations, each
+// lane rounded to nearest like its scalar form.
+__device__ __forceinline__ void add2_to(float& x, float& y, float a, float b) {
+    asm("{\n\t.reg .b64 p, q;\n\tmov.b64 p, {%0, %1};\n\tmov.b64 q, {%2, %3};\n\t"
+        "add.rn.f32x2 p, p, q;\n\tmov.b64 {%0, %1}, p;\n\t}"
+        : "+f"(x), "+f"(y) : "f"(a), "f"(b));
+}
+__device__ __forceinline__ float2 fma2(float x, float y, float a, float b, float c, float d) {
+    float2 r;
+    asm("{\n\t.reg .b64 p, q, w;\n\tmov.b64 p, {%2, %3};\n\tmov.b64 q, {%4, %5};\n\tmov.b64 w, {%6, %7};\n\t"
+        "fma.rn.f32x2 p, p, q, w;\n\tmov.b64 {%0, %1}, p;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "f"(x), "f"(y), "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -161,8 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    if (warp == kProducerWarp) {
-        if (lane == 0) {
+    if (warp >= kProducerWarp) {
+        regs_dec<kProducerRegs>();
+        if (warp == kProducerWarp && lane == 0) {
             tma_prefetch_desc(&tm_kv);
             const uint64_t pol = l2_policy_evict_first();
             uint32_t cnt = 0;
@@ -196,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 drain_wait(bar(B_FULL + i % NSTAGE), (i / NSTAGE) & 1u);
         }
     } else {
+        regs_inc<kConsumerRegs>();
         const int gi = warp / kGroupWarps, wq = warp % kGroupWarps;
         const int g = lane >> 2, c = lane & 3;
         const float sl2 = a.scale_log2;
@@ -285,19 +323,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float s[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    float4 t = sp[j * 32 + lane];
-#pragma unroll
-                    for (int w2 = 1; w2 < kGroupWarps; ++w2) {
-                        const float4 u = sp[(w2 * 4 + j) * 32 + lane];
-                        t.x += u.x;
-                        t.y += u.y;
-                        t.z += u.z;
-                        t.w += u.w;
-                    }
+                    const float4 t = sp[j * 32 + lane];
                     s[j][0] = t.x;
                     s[j][1] = t.y;
                     s[j][2] = t.z;
                     s[j][3] = t.w;
+#pragma unroll
+                    for (int w2 = 1; w2 < kGroupWarps; ++w2) {
+                        const float4 u = sp[(w2 * 4 + j) * 32 + lane];
+                        add2_to(s[j][0], s[j][1], u.x, u.y);
+                        add2_to(s[j][2], s[j][3], u.z, u.w);
+                    }
                 }
                 // 3. mask keys past each row's visible length; tile max per row
                 const int32_t tok0 = (2 * pc.t_begin + si) * ST;
@@ -319,58 +355,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                // 4. online softmax (exact: O rescaled whenever the max grows)
-                const float n0 = fmaxf(m0, mx0 * sl2), n1 = fmaxf(m1, mx1 * sl2);
-                const float f0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);   // exp2(-inf) = 0
-                const float f1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
-                const float neg0 = n0 == -INFINITY ? 0.f : -n0, neg1 = n1 == -INFINITY ? 0.f : -n1;
-                m0 = n0;
-                m1 = n1;
+                // 4. online softmax with a lazy maximum: the running max m (log2
+                //    units) moves, and O and l are rescaled, only when the tile
+                //    max exceeds it by more than 2^8; P = 2^(x - m) <= 2^8 then
+                //    (bf16 holds it exactly enough; O, l and m stay consistent)
+                const float t0 = mx0 * sl2, t1 = mx1 * sl2;
+                float f0 = 1.f, f1 = 1.f;
+                if (t0 > m0 + kRescaleThreshold) {
+                    if (m0 != -INFINITY) f0 = fast_exp2(m0 - t0);
+                    m0 = t0;
+                }
+                if (t1 > m1 + kRescaleThreshold) {
+                    if (m1 != -INFINITY) f1 = fast_exp2(m1 - t1);
+                    m1 = t1;
+                }
+                if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
+                    l0 *= f0;
+                    l1 *= f1;
+#pragma unroll
+                    for (int n = 0; n < kPvTiles; ++n) {
+                        o[n][0] *= f0;
+                        o[n][1] *= f0;
+                        o[n][2] *= f1;
+                        o[n][3] *= f1;
+                    }
+                }
+                const float neg0 = m0 == -INFINITY ? 0.f : -m0, neg1 = m1 == -INFINITY ? 0.f : -m1;
                 uint32_t pa[2][4];
-                float ls0 = 0.f, ls1 = 0.f;
+                float ls0 = 0.f, ls0b = 0.f, ls1 = 0.f, ls1b = 0.f;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float p00 = fast_exp2(fmaf(s[j][0], sl2, neg0));
-                    const float p01 = fast_exp2(fmaf(s[j][1], sl2, neg0));
-                    const float p10 = fast_exp2(fmaf(s[j][2], sl2, neg1));
-                    const float p11 = fast_exp2(fmaf(s[j][3], sl2, neg1));
-                    ls0 += p00 + p01;
-                    ls1 += p10 + p11;
+                    const float2 x0 = fma2(s[j][0], s[j][1], sl2, sl2, neg0, neg0);
+                    const float2 x1 = fma2(s[j][2], s[j][3], sl2, sl2, neg1, neg1);
+                    const float p00 = fast_exp2(x0.x), p01 = fast_exp2(x0.y);   // exp2(-inf) = 0
+                    const float p10 = fast_exp2(x1.x), p11 = fast_exp2(x1.y);
+                    add2_to(ls0, ls0b, p00, p01);
+                    add2_to(ls1, ls1b, p10, p11);
                     // n-tile j = tokens 8j..8j+7 -> k-step j/2, k half j&1
                     pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p00, p01);
                     pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p10, p11);
                 }
-                l0 = fmaf(l0, f0, ls0);
-                l1 = fmaf(l1, f1, ls1);
+                l0 += ls0 + ls0b;
+                l1 += ls1 + ls1b;
+                // 5. O += P V over this warp's 128 dims
+                if (tok0 + ST <= vis_hi) {
 #pragma unroll
-                for (int n = 0; n < kPvTiles; ++n) {
-                    o[n][0] *= f0;
-                    o[n][1] *= f0;
-                    o[n][2] *= f1;
-                    o[n][3] *= f1;
-                }
-                // 5. O += P V over this warp's 128 dims; cache rows past the
-                //    unit's last visible key are zeroed in the operand (P is
-                //    0 there, but the slot may hold anything)
-                const bool ragged = tok0 + ST > vis_hi;
+                    for (int kk2 = 0; kk2 < 2; ++kk2) {
+                        const uint32_t tok = 16u * kk2 + 8u * (((uint32_t)lane >> 3) & 1u) + ((uint32_t)lane & 7u);
 #pragma unroll
-                for (int kk2 = 0; kk2 < 2; ++kk2) {
-                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                    if (ragged) {
-                        const int32_t t = tok0 + 16 * kk2 + 2 * c;
-                        mlo = (t < vis_hi ? 0x0000ffffu : 0u) | (t + 1 < vis_hi ? 0xffff0000u : 0u);
-                        mhi = (t + 8 < vis_hi ? 0x0000ffffu : 0u) | (t + 9 < vis_hi ? 0xffff0000u : 0u);
+                        for (int np = 0; np < kPvTiles / 2; ++np) {
+                            // matrices: (k lo, n-tile 2np), (k hi, 2np), (k lo, 2np+1), (k hi, 2np+1)
+                            const uint32_t nt = 2u * np + ((uint32_t)lane >> 4);
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4_t(sb + chunk_off(2u * wq + (nt >> 3), tok, nt & 7u), b0, b1, b2, b3);
+                            mma16816(o[2 * np], pa[kk2], b0, b1);
+                            mma16816(o[2 * np + 1], pa[kk2], b2, b3);
+                        }
                     }
-                    const uint32_t tok = 16u * kk2 + 8u * (((uint32_t)lane >> 3) & 1u) + ((uint32_t)lane & 7u);
+                } else {
+                    // the unit's last stage: rows past its last visible key
+                    // are zeroed in the V operand (P is 0 there, but the
+                    // slot may hold anything)
 #pragma unroll
-                    for (int np = 0; np < kPvTiles / 2; ++np) {
-                        // matrices: (k lo, n-tile 2np), (k hi, 2np), (k lo, 2np+1), (k hi, 2np+1)
-                        const uint32_t nt = 2u * np + ((uint32_t)lane >> 4);
-                        const uint32_t box = 2u * wq + (nt >> 3);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(sb + chunk_off(box, tok, nt & 7u), b0, b1, b2, b3);
-                        mma16816(o[2 * np], pa[kk2], b0 & mlo, b1 & mhi);
-                        mma16816(o[2 * np + 1], pa[kk2], b2 & mlo, b3 & mhi);
+                    for (int kk2 = 0; kk2 < 2; ++kk2) {
+                        const int32_t t = tok0 + 16 * kk2 + 2 * c;
+                        const uint32_t mlo = (t < vis_hi ? 0x0000ffffu : 0u) | (t + 1 < vis_hi ? 0xffff0000u : 0u);
+                        const uint32_t mhi = (t + 8 < vis_hi ? 0x0000ffffu : 0u) | (t + 9 < vis_hi ? 0xffff0000u : 0u);
+                        const uint32_t tok = 16u * kk2 + 8u * (((uint32_t)lane >> 3) & 1u) + ((uint32_t)lane & 7u);
+#pragma unroll
+                        for (int np = 0; np < kPvTiles / 2; ++np) {
+                            const uint32_t nt = 2u * np + ((uint32_t)lane >> 4);
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4_t(sb + chunk_off(2u * wq + (nt >> 3), tok, nt & 7u), b0, b1, b2, b3);
+                            mma16816(o[2 * np], pa[kk2], b0 & mlo, b1 & mhi);
+                            mma16816(o[2 * np + 1], pa[kk2], b2 & mlo, b3 & mhi);
+                        }
                     }
                 }
                 __syncwarp();
@@ -468,6 +527,12 @@ cudaError_t launch_decode_sh(const CUtensorMap& kv, const ShArgs& a, int32_t num
                              const WsLayout& L, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(decode_sh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // the register split must fit what the launch allocates, or the
+    // consumers' setmaxnreg.inc could never be granted
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, decode_sh_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < 32 * (4 * kProducerRegs + 8 * kConsumerRegs)) return cudaErrorInvalidConfiguration;
     decode_sh_kernel<<<num_workers, kThreads, SMEM_BYTES, stream>>>(kv, a, ws, L);
     return cudaGetLastError();
 }
