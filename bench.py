@@ -386,6 +386,8 @@ def run_cuda(args, w):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     ev_att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_pre = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_post = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(dev) as clk:
         if dist is not None:
             dist.barrier()
@@ -404,15 +406,21 @@ def run_cuda(args, w):
     # the attention kernel alone (same inputs, same plan), for its roofline
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
+        ev_pre[i][0].record(stream)
         g_pre.replay()
+        ev_pre[i][1].record(stream)
         ev_att[i][0].record(stream)
         g_att.replay()
         ev_att[i][1].record(stream)
+        ev_post[i][0].record(stream)
         g_post.replay()
+        ev_post[i][1].record(stream)
         flush.zero_()
     torch.cuda.synchronize(dev)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     att_ms = [a.elapsed_time(b) for a, b in ev_att]
+    pre_ms = [a.elapsed_time(b) for a, b in ev_pre]
+    post_ms = [a.elapsed_time(b) for a, b in ev_post]
     tot_ms = max_over_ranks(sum(step_ms), dist, dev)
     status = mla.mla_decode_read_status(ws)
     if status != mla.MLA_OK:
@@ -550,9 +558,13 @@ def run_cuda(args, w):
         bound = "hbm" if t_mem >= t_tc else "tensor"
         achieved_gbs = alg_bytes / att_avg_s / 1e9
         achieved_tf = flops / att_avg_s / 1e12
-        traffic = (kernel_traffic("decode_tc_lowp_full_width.md" if args.lowp else "decode_tc_full_width.md",
-                                  "head_latent_attention_27_b300/csrc/decode_tc.cu")
-                   if w.name.startswith("full_width") else None)
+        if w.name.startswith("full_width"):
+            traffic = kernel_traffic("decode_tc_lowp_full_width.md" if args.lowp else "decode_tc_full_width.md",
+                                     "head_latent_attention_27_b300/csrc/decode_tc.cu")
+        elif w.name.startswith("small_head") and not args.lowp:
+            traffic = kernel_traffic("decode_sh_small_head.md", "head_latent_attention_27_b300/csrc/decode_sh.cu")
+        else:
+            traffic = None
         if bound == "hbm":
             roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                     "frac": achieved_gbs / hbm, "traffic": traffic}
@@ -596,6 +608,9 @@ def run_cuda(args, w):
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i (two buffer sets)",
                     "copies_only_ms_per_step": {"h2d": link_h2d, "d2h": link_d2h, "both": link_both},
                     "link_gbs": {"h2d": h2d / link_h2d / 1e6, "d2h": d2h / link_d2h / 1e6}},
+            "phases_ms": {"append_and_plan": statistics.median(pre_ms), "attend": statistics.median(att_ms),
+                          "combine": statistics.median(post_ms),
+                          "note": "each phase replayed as a graph of its own (no overlap between phases)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
