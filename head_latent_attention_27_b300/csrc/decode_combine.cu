@@ -20,8 +20,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     // here until that grid has completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const WsView v = ws_view(ws, L);
-    const int32_t u = blockIdx.x;
-    if (u >= v.hdr->num_units) return;
+    const int32_t u = blockIdx.x;   // the grid has exactly one block column per unit
     const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t QH = Q * H;
     const int32_t RB = units_per_seq(Q, H);
@@ -29,18 +28,29 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int32_t row = blockIdx.y * kWarpsPerBlock + warp;
     const int32_t rows_valid = min(kRowsPerUnit, QH - rb * kRowsPerUnit);
     if (row >= rows_valid) return;
-    const int32_t p0 = v.unit_piece_begin[u], p1 = v.unit_piece_begin[u + 1];
-    const int32_t n = p1 - p0;
+    const int32_t p0 = v.unit_piece_begin[u], n = v.unit_piece_begin[u + 1] - p0;
     if (n == 1) return;
     const int64_t grow = (int64_t)b * QH + (int64_t)rb * kRowsPerUnit + row;
 
+    // Every piece of the unit wrote finite partial rows, so the loads of the
+    // first two pieces' rows are issued together with the lse loads (one
+    // memory round trip instead of two); the weights are applied after.
     const float* lp = v.lse_part + (int64_t)p0 * kRowsPerUnit + row;   // lse of piece k: lp[k * 128]
-    // the lse of the first kCached pieces are loaded together (independent
-    // loads in flight), the rest, if any, one by one
-    constexpr int kCached = 8;
+    const float* ob = v.o_part + ((int64_t)p0 * kRowsPerUnit + row) * d_c;   // piece k: ob + k * 128 * d_c
+    const int64_t pstride = (int64_t)kRowsPerUnit * d_c;
+    constexpr int kChunks = 4;   // each lane owns up to 4 chunks of 4 columns (d_c <= 512, a multiple of 4)
+    constexpr int kCached = 8;   // the lse of the first kCached pieces are loaded together
     float lc[kCached];
 #pragma unroll
     for (int k = 0; k < kCached; ++k) lc[k] = k < n ? lp[(int64_t)k * kRowsPerUnit] : -INFINITY;
+    float4 x0[kChunks], x1[kChunks];
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+        const int32_t c0 = lane * 4 + 128 * j;
+        const bool in = c0 < d_c;
+        x0[j] = in && n > 0 ? *reinterpret_cast<const float4*>(ob + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x1[j] = in && n > 1 ? *reinterpret_cast<const float4*>(ob + pstride + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float m = -INFINITY;
 #pragma unroll
     for (int k = 0; k < kCached; ++k) m = fmaxf(m, lc[k]);
@@ -57,37 +67,37 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     float wc[kCached];
 #pragma unroll
     for (int k = 0; k < kCached; ++k)
-        wc[k] = (total_lse != -INFINITY && lc[k] != -INFINITY) ? expf(lc[k] - total_lse) : 0.f;
-    const float* ob = v.o_part + ((int64_t)p0 * kRowsPerUnit + row) * d_c;   // piece k: ob + k * 128 * d_c
-    const int64_t pstride = (int64_t)kRowsPerUnit * d_c;
-    // each lane owns up to 4 chunks of 4 columns (d_c <= 512, a multiple of
-    // 4); the loads of two pieces are issued before either is used
-    constexpr int kChunks = 4;
+        wc[k] = (k < n && total_lse != -INFINITY && lc[k] != -INFINITY) ? expf(lc[k] - total_lse) : 0.f;
     float4 acc[kChunks];
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // acc += w0 o_k0 + w1 o_k1, with both pieces' loads issued before use
+    for (int j = 0; j < kChunks; ++j) {
+        acc[j].x = wc[0] * x0[j].x + wc[1] * x1[j].x;
+        acc[j].y = wc[0] * x0[j].y + wc[1] * x1[j].y;
+        acc[j].z = wc[0] * x0[j].z + wc[1] * x1[j].z;
+        acc[j].w = wc[0] * x0[j].w + wc[1] * x1[j].w;
+    }
+    // acc += w0 o_k0 + w1 o_k1 for the remaining pieces, two at a time
     auto accumulate2 = [&](int32_t k0, float w0, int32_t k1, float w1) {
-        float4 x0[kChunks], x1[kChunks];
+        float4 y0[kChunks], y1[kChunks];
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
             const int32_t c0 = lane * 4 + 128 * j;
             const bool in = c0 < d_c;
-            x0[j] = in && w0 != 0.f ? *reinterpret_cast<const float4*>(ob + k0 * pstride + c0)
+            y0[j] = in && w0 != 0.f ? *reinterpret_cast<const float4*>(ob + k0 * pstride + c0)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            x1[j] = in && w1 != 0.f ? *reinterpret_cast<const float4*>(ob + k1 * pstride + c0)
+            y1[j] = in && w1 != 0.f ? *reinterpret_cast<const float4*>(ob + k1 * pstride + c0)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
-            acc[j].x += w0 * x0[j].x + w1 * x1[j].x;
-            acc[j].y += w0 * x0[j].y + w1 * x1[j].y;
-            acc[j].z += w0 * x0[j].z + w1 * x1[j].z;
-            acc[j].w += w0 * x0[j].w + w1 * x1[j].w;
+            acc[j].x += w0 * y0[j].x + w1 * y1[j].x;
+            acc[j].y += w0 * y0[j].y + w1 * y1[j].y;
+            acc[j].z += w0 * y0[j].z + w1 * y1[j].z;
+            acc[j].w += w0 * y0[j].w + w1 * y1[j].w;
         }
     };
 #pragma unroll
-    for (int k = 0; k < kCached; k += 2) {   // compile-time k: the weights stay in registers
+    for (int k = 2; k < kCached; k += 2) {   // compile-time k: the weights stay in registers
         if (k >= n) break;
         accumulate2(k, wc[k], k + 1 < n ? k + 1 : k, k + 1 < n ? wc[k + 1] : 0.f);
     }
