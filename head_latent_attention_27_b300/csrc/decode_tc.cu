@@ -23,8 +23,10 @@
 // Each accumulates its 256 output columns O += P V with P (bf16) in smem and
 // the same cache tile read as an MN-major V operand.
 //
-// Pipeline (per CTA, 480 threads):
+// Pipeline (per CTA, 512 threads):
 //   warp 0      TMA producer: q_rope per piece, 4-stage ring of cache tiles
+//               (low-precision rows: also expands the first half of each
+//               tile's codes to fp16)
 //   warp 1      QK issuer (owns TMEM): S(g) as soon as tile g has landed and
 //               its score buffer is free, up to two tiles ahead of the
 //               softmax
@@ -33,7 +35,8 @@
 //               handed between the groups, P -> smem, lazy O rescale,
 //               epilogue of a piece's last tile; q_nope -> TMEM
 //   warp 10     forwards "peer's scores read" to the peer (a slow remote
-//               arrive, kept off the softmax and swap warps)
+//               arrive, kept off the softmax and swap warps); low-precision
+//               rows: also expands the second half of each tile's codes
 //   warps 11-14 score swap: S(g) from TMEM -> fp16 -> st.async to the peer
 //   warp 15     PV issuer: O += P(g) V(g) as soon as P(g) is published, then
 //               frees the cache stage.  QK and PV are issued by different
@@ -71,9 +74,9 @@ constexpr uint32_t KN_BLK = BN * 128;                        // 64 dims x 64 tok
 constexpr uint32_t KR_BYTES = BN * 64;                       // 32 dims x 64 tokens, 64B swizzle
 constexpr uint32_t STAGE_BYTES = 4 * KN_BLK + KR_BYTES;      // 36864
 // Low-precision rows: per tile and CTA the 256 latent codes of 64 tokens
-// are loaded as two 128-byte-wide boxes into the tile's latent boxes 2 and 3
-// and expanded in place to fp16 (boxes 0..3); the 4 fp32 group scales of
-// each token go to a small ring of their own.
+// are loaded as two 128-byte-wide boxes into the tile's latent boxes 1 and 3
+// and expanded in place to fp16 (boxes 0-1 and 2-3, one half per warp); the
+// 4 fp32 group scales of each token go to a small ring of their own.
 constexpr uint32_t LP_CODE_BOX = BN * 128;                   // 64 tokens x 128 codes
 constexpr uint32_t LP_SCALE_BYTES = BN * 16;                 // 64 tokens x 4 fp32
 constexpr uint32_t LP_STAGE_TX = 2 * LP_CODE_BOX + LP_SCALE_BYTES + KR_BYTES;
@@ -251,13 +254,8 @@ struct TileCursor {
     }
 };
 
-// Dequantise one tile's low-precision latent codes in place (producer warp,
-// all 32 lanes): codes of latent dims [0,128) of this CTA's half sit in box
-// 2, dims [128,256) in box 3 ([64 tokens][128 codes], unswizzled); value =
-// E4M3(code) * group scale, written as fp16 into boxes 0..3 in the 128-byte
-// swizzled K-major layout the MMAs read.  The first half goes to boxes 0
-// and 1 (no overlap with any code); the second half's codes are all read
-// into registers before its outputs overwrite boxes 2 and 3.
+// One 16-byte chunk of codes (16 latent dims c8*16.. of one token row) ->
+// fp16 values in the swizzled K-major layout of boxes box0 and box0+1.
 __device__ __forceinline__ void expand16(uint8_t* ring, uint32_t st, uint32_t box0, int row, int c8, uint4 cw,
                                          float sc) {
     const __half2 s2 = __float2half2_rn(sc);
@@ -281,34 +279,39 @@ __device__ __forceinline__ void expand16(uint8_t* ring, uint32_t st, uint32_t bo
     *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ sw) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-__device__ __forceinline__ void dequant_tile(uint8_t* ring, uint32_t st, const float* scales, uint32_t rank,
-                                             int lane) {
-    // All 16 chunks of codes (and their scales) of a half are loaded before
-    // any is expanded: the loads then overlap instead of each one waiting
-    // behind the previous chunk's stores (the compiler cannot reorder shared
-    // loads above possibly aliasing shared stores).  The second half's codes
-    // sit in box 3, which its outputs overwrite: all lanes have read them
-    // (__syncwarp) before the first store.
+// Dequantise half of one tile's low-precision latent codes in place (one
+// warp, all 32 lanes).  Half h holds this CTA's latent dims [128h, 128h+128):
+// its codes ([64 tokens][128 codes], unswizzled) sit in box 2h+1 and expand,
+// value = E4M3(code) * group scale, into fp16 boxes 2h and 2h+1 in the
+// 128-byte swizzled K-major layout the MMAs read.  The two halves touch
+// disjoint boxes, so two warps expand them concurrently.  Within a half, the
+// fp16 values of token row r overwrite only row r's own codes (bytes
+// [128r, 128r+128) of box 2h+1), so rows are expanded in batches: a batch's
+// codes are all read (and the warp synchronised) before its first store,
+// and later batches read other rows.
+__device__ __forceinline__ void dequant_half(uint8_t* ring, uint32_t st, const float* scales, uint32_t rank,
+                                             int lane, int half) {
+    const uint8_t* codes = ring + nope_box(st, 2 * half + 1);
+    constexpr int kBatch = 8;   // 8 x 32 chunks of 16 codes = 32 token rows per batch
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        const uint8_t* codes = ring + nope_box(st, 2 + half);
-        uint4 cw[16];
-        float sc[16];
+    for (int b0 = 0; b0 < 16; b0 += kBatch) {
+        uint4 cw[kBatch];
+        float sc[kBatch];
 #pragma unroll
-        for (int it = 0; it < 16; ++it) {
-            const int pidx = it * 32 + lane;           // 512 chunks of 16 codes per half
+        for (int i = 0; i < kBatch; ++i) {
+            const int pidx = (b0 + i) * 32 + lane;   // 512 chunks of 16 codes per half
             const int row = pidx >> 3;
-            cw[it] = *reinterpret_cast<const uint4*>(codes + row * 128 + (pidx & 7) * 16);
-            sc[it] = scales[row * 4 + 2 * rank + half];
+            cw[i] = *reinterpret_cast<const uint4*>(codes + row * 128 + (pidx & 7) * 16);
+            sc[i] = scales[row * 4 + 2 * rank + half];
         }
         __syncwarp();
 #pragma unroll
-        for (int it = 0; it < 16; ++it) {
-            const int pidx = it * 32 + lane;
-            expand16(ring, st, 2 * half, pidx >> 3, pidx & 7, cw[it], sc[it]);
+        for (int i = 0; i < kBatch; ++i) {
+            const int pidx = (b0 + i) * 32 + lane;
+            expand16(ring, st, 2 * half, pidx >> 3, pidx & 7, cw[i], sc[i]);
         }
+        __syncwarp();
     }
-    __syncwarp();
 }
 
 template <bool kLowp>
@@ -336,7 +339,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(bar(B_QREMPTY), 1);
         mbar_init(bar(B_QNFULL), 4);
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(bar(B_KVFULL + s), 1);
+            mbar_init(bar(B_KVFULL + s), kLowp ? 2 : 1);   // low-precision: the two expander warps
             mbar_init(bar(B_KVEMPTY + s), 1);
             mbar_init(bar(B_LPFULL + s), 1);
         }
@@ -380,12 +383,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int32_t max_tokens = a.max_pages_per_seq * kTileTokens;
 
     if (warp == 0 && kLowp) {
-        // -------------------------------- TMA producer + in-place dequantiser
+        // ------------------------ TMA producer + in-place dequantiser (half 0)
         // One loop, never blocking on one condition while the other could
         // progress: lane 0 issues the loads of the next tile as soon as its
         // stage is free (and, at a piece's first tile, the previous piece has
-        // released q_rope); the whole warp expands the oldest landed tile and
-        // marks it full for the MMAs.  Gives up (timeout status) after the
+        // released q_rope); the whole warp expands the first half of the
+        // oldest landed tile and marks it for the MMAs (the forwarder warp
+        // expands the second half; the tile is full after both).  Gives up (timeout status) after the
         // same time limit as every other wait when neither can progress.
         const uint64_t pol = a.evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
         uint8_t* ring = smem + OFF_KV;
@@ -420,7 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint32_t fb = bar(B_LPFULL + st);
                         mbar_arrive_expect_tx(fb, LP_STAGE_TX);
                         const int32_t y0 = page * BN;
-                        tma_load_2d(sbase + OFF_KV + nope_box(st, 2), &tm_kv_nope, fb, 256 * rank, y0, pol);
+                        tma_load_2d(sbase + OFF_KV + nope_box(st, 1), &tm_kv_nope, fb, 256 * rank, y0, pol);
                         tma_load_2d(sbase + OFF_KV + nope_box(st, 3), &tm_kv_nope, fb, 256 * rank + 128, y0, pol);
                         tma_load_2d(sbase + OFF_SC + st * LP_SCALE_BYTES, &tm_kv_scale, fb, 128, y0, pol);
                         tma_load_2d(sbase + OFF_KV + rope_box(st), &tm_kv_rope, fb, 264 + 32 * rank, y0, pol);
@@ -437,8 +441,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t st = expanded % NSTAGE, ph = (expanded / NSTAGE) & 1u;
                 const int landed = lane == 0 ? (mbar_try_wait(bar(B_LPFULL + st), ph) ? 1 : 0) : 0;
                 if (__shfl_sync(0xffffffffu, landed, 0)) {
-                    dequant_tile(ring, st, reinterpret_cast<const float*>(smem + OFF_SC + st * LP_SCALE_BYTES),
-                                 rank, lane);
+                    dequant_half(ring, st, reinterpret_cast<const float*>(smem + OFF_SC + st * LP_SCALE_BYTES),
+                                 rank, lane, 0);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B_KVFULL + st));
@@ -905,6 +909,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_OFREE));   // O may be overwritten by the next piece
+            }
+        }
+    } else if (warp == kForwardWarp && kLowp) {
+        // ---------- "scores read" forwarder + in-place dequantiser (half 1)
+        // The forwarding below, polled instead of blocking so that the warp
+        // also expands the second half of every landed low-precision tile.
+        uint8_t* ring = smem + OFF_KV;
+        const uint32_t peerfree_remote0 = map_to_cta(bar(B_PEERFREE), peer);
+        uint32_t total = 0;
+        for (int32_t p = p_begin; p < p_end; ++p) total += (uint32_t)(v.pieces[p].t_end - v.pieces[p].t_begin);
+        uint32_t fwd = 0, expanded = 0;
+        bool ok = true;
+        uint64_t idle_since = 0;
+        while (ok && (fwd < total || expanded < total)) {
+            bool progressed = false;
+            if (fwd < total) {
+                int done = 0;
+                if (lane == 0 && mbar_try_wait(bar(B_XREAD + (fwd & 1u)), (fwd >> 1) & 1u)) {
+                    mbar_arrive_remote(peerfree_remote0 + 8u * (fwd & 1u));
+                    done = 1;
+                }
+                if (__shfl_sync(0xffffffffu, done, 0)) {
+                    ++fwd;
+                    progressed = true;
+                }
+            }
+            if (expanded < total) {
+                const uint32_t st = expanded % NSTAGE, ph = (expanded / NSTAGE) & 1u;
+                const int landed = lane == 0 ? (mbar_try_wait(bar(B_LPFULL + st), ph) ? 1 : 0) : 0;
+                if (__shfl_sync(0xffffffffu, landed, 0)) {
+                    dequant_half(ring, st, reinterpret_cast<const float*>(smem + OFF_SC + st * LP_SCALE_BYTES),
+                                 rank, lane, 1);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_KVFULL + st));
+                    ++expanded;
+                    progressed = true;
+                }
+            }
+            if (progressed) {
+                idle_since = 0;
+            } else {
+                __nanosleep(32);
+                const uint64_t now = global_timer_ns();
+                if (idle_since == 0) idle_since = now;
+                int stop = 0;
+                if (lane == 0 && (*abort_flag || now - idle_since > kWaitLimitNs)) {
+                    if (!*abort_flag) {
+                        *abort_flag = 1;
+                        atomicExch(status, 4 /* MLA_ERR_TIMEOUT */);
+                    }
+                    stop = 1;
+                }
+                if (__shfl_sync(0xffffffffu, stop, 0)) ok = false;
             }
         }
     } else if (warp == kForwardWarp) {
