@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(128, 1)
     constexpr uint32_t STAGE_BYTES = Tile<BN>::STAGE_BYTES;
     constexpr uint32_t TM_COLS = Tile<BN>::TM_COLS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_smem_1024(smem_raw);
     const uint32_t sbase = smem_addr(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t mt = blockIdx.x, h = blockIdx.y, nt = blockIdx.z;

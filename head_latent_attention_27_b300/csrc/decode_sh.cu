@@ -171,7 +171,7 @@ __device__ __forceinline__ uint32_t chunk_off(uint32_t box, uint32_t tok, uint32
 __global__ void __launch_bounds__(kThreads, 1)
     decode_sh_kernel(const __grid_constant__ CUtensorMap tm_kv, const ShArgs a, void* ws, const WsLayout L) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_smem_1024(smem_raw);
     const uint32_t sbase = smem_addr(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;

@@ -320,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_q_rope, const __grid_constant__ CUtensorMap tm_kv_scale,
                      const TcArgs a, void* ws, const WsLayout L) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_smem_1024(smem_raw);
     const uint32_t sbase = smem_addr(smem);
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(UP_THREADS, 1)
     upproj_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_wk,
                   const __grid_constant__ CUtensorMap tm_wv, const UpprojArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_smem_1024(smem_raw);
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) -> uint32_t { return sbase + UP_OFF_BAR + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + UP_OFF_BAR + 256 - 16);
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_kr, const PrefillAttnArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_smem_1024(smem_raw);
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int i) -> uint32_t { return sbase + AT_OFF_BAR + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AT_OFF_BAR + 256 - 16);

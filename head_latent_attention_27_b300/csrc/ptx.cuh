@@ -16,6 +16,15 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Base of dynamic shared memory rounded up to 1024 bytes (the alignment of
+// 128-byte swizzle atoms).  Computed by pointer arithmetic on the shared
+// array itself, so that accesses through the result are known to be
+// shared-memory accesses (a round trip through an integer would leave them
+// as generic accesses).
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* raw) {
+    return raw + ((1024u - (smem_addr(raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
