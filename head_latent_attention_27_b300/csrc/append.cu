@@ -54,10 +54,21 @@ __global__ void __launch_bounds__(kWarps * 32)
     // latent: optional RMSNorm
     float inv_rms = 1.f;
     if (a.flags & 1u) {
+        // sum of squares: lane k sums its contiguous block of d_c/32
+        // elements in order (the order of the 576-wide and low-precision
+        // kernels), strided when d_c is not a multiple of 32
         float ss = 0.f;
-        for (int32_t k = lane; k < a.d_c; k += 32) {
-            const float v = load_f(x + k);
-            ss = fmaf(v, v, ss);
+        if (a.d_c % 32 == 0) {
+            const int32_t per = a.d_c >> 5;
+            for (int32_t i = 0; i < per; ++i) {
+                const float v = load_f(x + lane * per + i);
+                ss = fmaf(v, v, ss);
+            }
+        } else {
+            for (int32_t k = lane; k < a.d_c; k += 32) {
+                const float v = load_f(x + k);
+                ss = fmaf(v, v, ss);
+            }
         }
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
@@ -88,6 +99,82 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 }
 
+// RoPE rotation of pair i = (x0, x1) at position pos (flags bit 2), angle
+// reduced modulo 2 pi in fp64 as described at the top of the file.
+__device__ __forceinline__ void rope_pair(const AppendArgs& a, int32_t pos, int32_t i, float x0, float x1,
+                                          float& y0, float& y1) {
+    y0 = x0;
+    y1 = x1;
+    if (a.flags & 2u) {
+        constexpr double kTwoPi = 6.283185307179586476925286766559;
+        const double ang = (double)pos * a.theta[i];
+        const double r = fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);   // in [-pi, pi]
+        float sf, cf;
+        sincosf((float)r, &sf, &cf);
+        y0 = x0 * cf - x1 * sf;
+        y1 = x0 * sf + x1 * cf;
+    }
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* v) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __uint_as_float(w[j] << 16);
+        v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// The bf16-input, bf16-cache append at the 576-wide row (d_c = 512,
+// d_r = 64): lane k owns latent elements [16k, 16k + 16) (two 16-byte loads
+// and stores) and RoPE pair k (one 4-byte load and store).  The token's
+// inputs are loaded before its page is looked up, so their latency overlaps
+// the index loads.  Sum of squares: each lane's 16 terms in order, then a
+// butterfly over the lanes (the low-precision append uses the same order,
+// so both form the same bf16 row).
+__global__ void __launch_bounds__(kWarps * 32)
+    append_bf16_row_kernel(AppendArgs a, const __nv_bfloat16* __restrict__ ckv, const __nv_bfloat16* __restrict__ kr,
+                           __nv_bfloat16* __restrict__ cache) {
+    const int32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int32_t lane = threadIdx.x & 31;
+    if (t >= a.T) return;
+    const uint4* xv = reinterpret_cast<const uint4*>(ckv + (int64_t)t * 512) + 2 * lane;
+    const uint4 u0 = xv[0], u1 = xv[1];
+    const uint32_t kp = reinterpret_cast<const uint32_t*>(kr + (int64_t)t * 64)[lane];
+    const int32_t b = a.seq_ids[t], pos = a.positions[t];
+    if (b < 0 || b >= a.num_seqs || pos < 0 || pos >= a.max_pages_per_seq * a.page_size) return;
+    const int32_t page = a.page_table[(int64_t)b * a.max_pages_per_seq + pos / a.page_size];
+    if (page < 0 || page >= a.num_pages) return;
+    __nv_bfloat16* row = cache + ((int64_t)page * a.page_size + pos % a.page_size) * 576;
+
+    float v[16];
+    unpack_bf16x8(u0, v);
+    unpack_bf16x8(u1, v + 8);
+    if (a.flags & 1u) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, d);
+        const float inv_rms = 1.f / sqrtf(ss / 512.f + a.eps);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = v[i] * inv_rms * (a.gamma ? a.gamma[16 * lane + i] : 1.f);
+    }
+    uint4* rv = reinterpret_cast<uint4*>(row) + 2 * lane;
+    rv[0] = make_uint4(pack_bf16x2_rn(v[0], v[1]), pack_bf16x2_rn(v[2], v[3]), pack_bf16x2_rn(v[4], v[5]),
+                       pack_bf16x2_rn(v[6], v[7]));
+    rv[1] = make_uint4(pack_bf16x2_rn(v[8], v[9]), pack_bf16x2_rn(v[10], v[11]), pack_bf16x2_rn(v[12], v[13]),
+                       pack_bf16x2_rn(v[14], v[15]));
+    float y0, y1;
+    rope_pair(a, pos, lane, __uint_as_float(kp << 16), __uint_as_float(kp & 0xffff0000u), y0, y1);
+    reinterpret_cast<uint32_t*>(row + 512)[lane] = pack_bf16x2_rn(y0, y1);
+}
+
 // Low-precision cache row (656 bytes): the 512 latent values as E4M3 codes,
 // one fp32 scale per 128-element group, then the RoPE key in bf16.  The row
 // is first formed exactly as for the bf16 cache (same arithmetic and
@@ -110,10 +197,11 @@ __global__ void __launch_bounds__(kWarps * 32)
     const Tin* x = ckv + (int64_t)t * kFp8Dc;
 
     float inv_rms = 1.f;
-    if (a.flags & 1u) {   // same summation order as the bf16 row
+    if (a.flags & 1u) {   // same summation order as the bf16 row: lane k's 16 elements, then the lanes
         float ss = 0.f;
-        for (int32_t k = lane; k < kFp8Dc; k += 32) {
-            const float v = load_f(x + k);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float v = load_f(x + 16 * lane + i);
             ss = fmaf(v, v, ss);
         }
 #pragma unroll
@@ -186,7 +274,13 @@ cudaError_t launch_append(const AppendArgs& a, const void* ckv, const void* kr, 
                                                                  static_cast<uint8_t*>(cache));
         return cudaGetLastError();
     }
-    if (in_dtype == 0 && cache_dtype == 0)
+    const bool aligned = ((reinterpret_cast<uintptr_t>(ckv) | reinterpret_cast<uintptr_t>(cache)) & 15u) == 0 &&
+                         (reinterpret_cast<uintptr_t>(kr) & 3u) == 0;
+    if (in_dtype == 0 && cache_dtype == 0 && a.d_c == 512 && a.d_r == 64 && aligned)
+        append_bf16_row_kernel<<<grid, block, 0, stream>>>(a, static_cast<const __nv_bfloat16*>(ckv),
+                                                           static_cast<const __nv_bfloat16*>(kr),
+                                                           static_cast<__nv_bfloat16*>(cache));
+    else if (in_dtype == 0 && cache_dtype == 0)
         append_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, block, 0, stream>>>(
             a, static_cast<const __nv_bfloat16*>(ckv), static_cast<const __nv_bfloat16*>(kr),
             static_cast<__nv_bfloat16*>(cache));

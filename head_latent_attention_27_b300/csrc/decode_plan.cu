@@ -13,6 +13,12 @@ namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+// The per-unit tile counts and costs and the piece -> worker map are only
+// read inside the plan; when they are small enough they stay in shared
+// memory (the passes read them back there instead of from global memory,
+// and the last pass's binary searches run over shared memory).
+constexpr int kSmemUnits = 2048;
+constexpr int kSmemPieces = 4096;
 
 // Exclusive scan over the block; returns the exclusive prefix of `v` and
 // writes the block total to *total.  All threads must call it.
@@ -53,6 +59,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     WsView v = ws_view(ws, L);
     const int32_t RB = units_per_seq(Q, H);
     const int32_t U = B * RB;
+    __shared__ int32_t s_tiles[kSmemUnits], s_cost[kSmemUnits], s_pw[kSmemPieces];
+    int32_t* unit_tiles = U <= kSmemUnits ? s_tiles : v.unit_tiles;
+    int32_t* unit_cost = U <= kSmemUnits ? s_cost : v.unit_cost;
     const int32_t QH = Q * H;
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -88,8 +97,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         const int64_t ex_cost = block_exclusive_scan(cost, &tot_cost);
         const int64_t ex_np = block_exclusive_scan(np, &tot_np);
         if (u < U) {
-            v.unit_tiles[u] = (int32_t)tiles;
-            v.unit_cost[u] = (int32_t)(carry_cost + ex_cost);
+            unit_tiles[u] = (int32_t)tiles;
+            unit_cost[u] = (int32_t)(carry_cost + ex_cost);
             if (n_split > 0) v.unit_piece_begin[u] = (int32_t)(carry_np + ex_np);
         }
         carry_cost += tot_cost;
@@ -106,9 +115,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             const int32_t u = base + tid;
             int64_t np = 0;
             if (u < U) {
-                const int64_t tiles = v.unit_tiles[u];
+                const int64_t tiles = unit_tiles[u];
                 if (tiles > 0) {
-                    const int64_t a = (int64_t)v.unit_cost[u] + kPieceOverheadTiles;
+                    const int64_t a = (int64_t)unit_cost[u] + kPieceOverheadTiles;
                     np = (a + tiles - 1) / T - a / T + 1;
                 }
             }
@@ -119,6 +128,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         }
     }
     const int64_t NP = carry_np;
+    int32_t* piece_worker = NP <= kSmemPieces ? s_pw : v.piece_worker;
     if (tid == 0) {
         v.unit_piece_begin[U] = (int32_t)NP;
         v.hdr->num_pieces = (int32_t)NP;
@@ -127,11 +137,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
     // Pass 3: write the pieces (one thread per unit).
     for (int32_t u = tid; u < U; u += kPlanThreads) {
-        const int32_t tiles = v.unit_tiles[u];
+        const int32_t tiles = unit_tiles[u];
         if (tiles == 0) continue;
         const int32_t p0 = v.unit_piece_begin[u];
         const int32_t np = v.unit_piece_begin[u + 1] - p0;
-        const int64_t a = v.unit_cost[u];
+        const int64_t a = unit_cost[u];
         if (n_split > 0) {
             const int32_t chunk = (int32_t)ceil_div64(tiles, n_split);
             for (int32_t k = 0; k < np; ++k) {
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                 pc.slot = np > 1 ? p0 + k : -1;
                 v.pieces[p0 + k] = pc;
                 const int64_t start = a + (int64_t)k * (chunk + kPieceOverheadTiles);
-                v.piece_worker[p0 + k] = (int32_t)(start / T < (int64_t)(P - 1) ? start / T : (int64_t)(P - 1));
+                piece_worker[p0 + k] = (int32_t)(start / T < (int64_t)(P - 1) ? start / T : (int64_t)(P - 1));
             }
         } else {
             const int64_t a0 = a + kPieceOverheadTiles;
@@ -155,7 +165,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                 pc.t_end = (int32_t)((c + 1) * T - a0 < (int64_t)tiles ? (c + 1) * T - a0 : (int64_t)tiles);
                 pc.slot = np > 1 ? p0 + k : -1;
                 v.pieces[p0 + k] = pc;
-                v.piece_worker[p0 + k] = (int32_t)c;
+                piece_worker[p0 + k] = (int32_t)c;
             }
         }
     }
@@ -166,7 +176,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         int64_t lo = 0, hi = NP;
         while (lo < hi) {
             const int64_t mid = (lo + hi) >> 1;
-            if (v.piece_worker[mid] < c) lo = mid + 1; else hi = mid;
+            if (piece_worker[mid] < c) lo = mid + 1; else hi = mid;
         }
         v.worker_begin[c] = (int32_t)lo;
     }
