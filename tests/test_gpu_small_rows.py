@@ -93,3 +93,27 @@ def test_small_unit_bad_length_is_reported():
     mla.mla_decode(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, lse=lse, workspace=ws)
     assert mla.mla_decode_read_status(ws) == mla.MLA_ERR_INVALID_ARG
     assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+
+
+def test_small_unit_one_plan_serves_several_attention_launches():
+    """A caller decoding several layers with the same lengths plans once and
+    runs the attention kernel per layer; split units must merge every time."""
+    import math
+    mla = mla_pkg()
+    w = synth.custom_bf16("h16_plan_reuse", 936, [4096, 4096, 700, 64, 3001, 1], H=16, Q=1, paged=True)
+    cache, d = build_cache(w)
+    scale = 1.0 / math.sqrt(w.d_h + w.d_r)
+    ws = mla.alloc_workspace(w.B, w.Q, w.H, w.d_c, 0, "cuda")
+    mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws)
+    outs = []
+    for _ in range(3):
+        out = torch.full((w.B, w.Q, w.H, w.d_c), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((w.B, w.Q, w.H), float("nan"), dtype=torch.float32, device="cuda")
+        mla.mla_decode_attend(cache, d["seq_lens"], d["q_nope"], d["q_rope"], out, ws, lse=lse, softmax_scale=scale)
+        mla.mla_decode_combine(cache, out, ws, lse=lse)
+        assert mla.mla_decode_read_status(ws) == mla.MLA_OK
+        outs.append((out.double().cpu().numpy(), lse.double().cpu().numpy()))
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+    compare(w, *outs[0])
+
