@@ -7,8 +7,8 @@ import torch
 
 import oracle as O
 import synth
-from gpu_util import build_cache, compare, mla_pkg, run_decode
-from synth.device import to_torch
+from gpu_util import append_flags, build_cache, compare, mla_pkg, run_decode
+from synth.device import empty_pool, to_torch, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +41,31 @@ def test_append_places_rows_bit_exactly_and_within_one_ulp():
     ulp = np.abs(_ordered(pool[written_ref]) - _ordered(ref_bits))
     assert ulp.max() <= 1, ulp.max()
     assert np.mean(ulp == 0) > 0.99
+
+
+def test_append_vector_and_scalar_kernels_write_the_same_rows():
+    """The 576-wide bf16 append uses 16-byte accesses when its inputs are
+    16-byte aligned and the general kernel otherwise; both must write the
+    same bits (same arithmetic and summation order)."""
+    mla = mla_pkg()
+    w = synth.custom_bf16("append_align", 502, [1, 63, 64, 65, 130, 257], H=4, paged=True)
+    d = upload(w, "cuda")
+    T = d["raw_c"].shape[0]
+    pools = []
+    for offset in (0, 1):   # offset 1: the inputs start 2 bytes past a 16-byte boundary
+        big_c = torch.zeros(T * w.d_c + 8, dtype=torch.bfloat16, device="cuda")
+        big_k = torch.zeros(T * w.d_r + 8, dtype=torch.bfloat16, device="cuda")
+        c_in = big_c[offset:offset + T * w.d_c].view(T, w.d_c)
+        k_in = big_k[offset:offset + T * w.d_r].view(T, w.d_r)
+        c_in.copy_(d["raw_c"])
+        k_in.copy_(d["raw_k"])
+        pool = empty_pool(w, "cuda", fill_nan=True)
+        cache = mla.Cache(pool, d["page_table"], w.d_c, w.d_r)
+        mla.mla_cache_append(cache, c_in, k_in, d["seq_ids"], d["positions"], eps=w.eps, rope_base=w.rope_base,
+                             flags=append_flags(mla, w))
+        torch.cuda.synchronize()
+        pools.append(pool.view(torch.int16).cpu().numpy())
+    assert np.array_equal(pools[0], pools[1])
 
 
 @pytest.mark.parametrize("positions", [[0, 4095, 4096, 131071]])
