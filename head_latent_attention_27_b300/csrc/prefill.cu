@@ -12,13 +12,17 @@
 // tile, head) item at a time, by groups of heads, heaviest items (last
 // query tiles) first within a group.
 // Warp 0 loads the item's queries [q^C || q^R] (128 x 192) and, per
-// 128-key tile, the keys [K^C || k^R] (128 x 192) and values (128 x 128)
-// into a 2-stage ring; warp 1 issues S = Q K^T (12 MMAs, N=128) into one of
-// two TMEM score buffers and O += P V (8 MMAs, A = P read from TMEM);
-// warps 2-5 (one thread per query row) run the online softmax in fp32:
-// causal mask on the diagonal tile, running maximum with a lazy O rescale
-// (only when the maximum grows by more than 2^8), P written back as bf16
-// into the score buffer's first 64 columns, and the epilogue O / l.
+// 128-key tile, the keys [K^C || k^R] (128 x 192) into a 2-stage key ring;
+// warp 2 loads the values (128 x 128) into a 2-stage value ring (a key stage
+// is free as soon as its QK completes, a value stage only after its PV);
+// warp 1 issues S = Q K^T (12 MMAs, N=128) into one of two TMEM score
+// buffers and O += P V (8 MMAs, A = P read from TMEM);
+// two softmax warpgroups (warps 4-7 and 8-11, one thread per query row)
+// take alternate key tiles and run the online softmax in fp32: causal mask
+// on the diagonal tile, running maximum handed from one group to the other
+// with a lazy O rescale (only when the maximum grows by more than 2^8), P
+// written back as bf16 into the score buffer's first 64 columns; the owner
+// of an item's last tile merges both groups' row sums and writes O / l.
 // TMEM: S0 128 columns | S1 128 | O 128.
 //
 // Every wait is bounded (ptx.cuh: bounded_wait); on a timeout the kernel
@@ -241,25 +245,43 @@ constexpr uint32_t BOX = 128 * 128;                       // one [128 rows][64 b
 constexpr uint32_t AT_Q_BYTES = 3 * BOX;                  // q^C (2 boxes) || q^R
 constexpr uint32_t AT_K_BYTES = 3 * BOX;                  // K^C (2 boxes) || k^R (two 8 KB page boxes)
 constexpr uint32_t AT_V_BYTES = 2 * BOX;
-constexpr uint32_t AT_STAGE = AT_K_BYTES + AT_V_BYTES;    // 80 KB
 constexpr int AT_NST = 2;
 constexpr uint32_t AT_OFF_Q = 0;
-constexpr uint32_t AT_OFF_KV = AT_Q_BYTES;
-constexpr uint32_t AT_OFF_BAR = AT_OFF_KV + AT_NST * AT_STAGE;
-constexpr uint32_t AT_SMEM = AT_OFF_BAR + 256 + 1024;
+// Keys and values of a key tile sit in separate rings: a key stage is free
+// once its QK has completed, a value stage once its PV has.
+constexpr uint32_t AT_OFF_K = AT_Q_BYTES;
+constexpr uint32_t AT_OFF_V = AT_OFF_K + AT_NST * AT_K_BYTES;
+constexpr uint32_t AT_OFF_BAR = AT_OFF_V + AT_NST * AT_V_BYTES;
+constexpr uint32_t AT_OFF_M = AT_OFF_BAR + 256;              // [2 slots][128 rows] running max after a tile
+constexpr uint32_t AT_OFF_LM = AT_OFF_M + 2 * 128 * 4;       // [2][128] (row sum, its max) of a group
+constexpr uint32_t AT_SMEM = AT_OFF_LM + 2 * 128 * 8 + 1024;
 static_assert(AT_SMEM <= 232448, "fits in 227 KB");
-constexpr int AT_THREADS = 192;
+// Three warpgroups: warp 0 TMA, warp 1 MMA (warps 2-3 idle), and two
+// softmax warpgroups (warps 4-7, 8-11) taking alternate key tiles.  The
+// producer warpgroup hands most of its registers to the softmax groups
+// (setmaxnreg), whose 128 scores per thread would not fit the 168
+// registers of a 384-thread launch; the shares add up to 384 x 168 and the
+// launcher checks the compiled count before every launch.
+constexpr int AT_THREADS = 384;
+constexpr int AT_PRODUCER_REGS = 56;
+constexpr int AT_SOFTMAX_REGS = 224;
+static_assert(4 * AT_PRODUCER_REGS + 8 * AT_SOFTMAX_REGS <= 12 * 168, "register split within the launch");
 enum : int {
     A_QFULL = 0,
     A_QEMPTY,
-    A_KVFULL,
-    A_KVEMPTY = A_KVFULL + AT_NST,
-    A_SFULL = A_KVEMPTY + AT_NST,   // [2]
+    A_KFULL,
+    A_KEMPTY = A_KFULL + AT_NST,
+    A_VFULL = A_KEMPTY + AT_NST,
+    A_VEMPTY = A_VFULL + AT_NST,
+    A_SFULL = A_VEMPTY + AT_NST,    // [2]
     A_PFULL = A_SFULL + 2,          // [2]
     A_PVDONE = A_PFULL + 2,         // [2] PV of the tile in that slot completed
     A_OFREE = A_PVDONE + 2,         // epilogue read O
     A_EXIT,
-    A_NBARS
+    A_MREADY,                       // [2] running max after the tile in that slot published
+    A_LFULL = A_MREADY + 2,         // [2] a group's row sum of an item published (item parity)
+    A_LFREE = A_LFULL + 2,          // [2] ... and read by the epilogue group
+    A_NBARS = A_LFREE + 2
 };
 static_assert(A_NBARS * 8 + 16 <= 256, "barrier area");
 constexpr uint32_t TM_S0 = 0, TM_O = 256;
@@ -304,8 +326,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_init(bar(A_QFULL), 1);
         mbar_init(bar(A_QEMPTY), 1);
         for (int s = 0; s < AT_NST; ++s) {
-            mbar_init(bar(A_KVFULL + s), 1);
-            mbar_init(bar(A_KVEMPTY + s), 1);
+            mbar_init(bar(A_KFULL + s), 1);
+            mbar_init(bar(A_KEMPTY + s), 1);
+            mbar_init(bar(A_VFULL + s), 1);
+            mbar_init(bar(A_VEMPTY + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(A_SFULL + s), 1);
@@ -314,6 +338,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         mbar_init(bar(A_OFREE), 4);
         mbar_init(bar(A_EXIT), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(A_MREADY + s), 4);
+            mbar_init(bar(A_LFULL + s), 4);
+            mbar_init(bar(A_LFREE + s), 4);
+        }
         *abort_flag = 0;
         fence_mbar_init_cluster();
     }
@@ -336,6 +365,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int32_t m_tiles = (a.T + AT_BM - 1) / AT_BM;
     const int32_t items = m_tiles * a.H;
 
+    if (warp < 4) {
+    // producer warpgroup: the register budget of the code below is set here
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(AT_PRODUCER_REGS));
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
@@ -353,11 +385,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 tma_load_2d(sbase + AT_OFF_Q + 2 * BOX, &tm_qr, bar(A_QFULL), it.h * kPrefillDr, y, pol);
                 ++qn;
                 for (int32_t j = 0; j < it.ntiles; ++j) {
-                    ok = bounded_wait(bar(A_KVEMPTY + stage), phase ^ 1u, abort_flag, a.status);
+                    ok = bounded_wait(bar(A_KEMPTY + stage), phase ^ 1u, abort_flag, a.status);
                     if (!ok) break;
-                    const uint32_t fb = bar(A_KVFULL + stage);
-                    const uint32_t dst = sbase + AT_OFF_KV + stage * AT_STAGE;
-                    mbar_arrive_expect_tx(fb, AT_STAGE);
+                    const uint32_t fb = bar(A_KFULL + stage);
+                    const uint32_t dst = sbase + AT_OFF_K + stage * AT_K_BYTES;
+                    mbar_arrive_expect_tx(fb, AT_K_BYTES);
                     const int32_t yk = j * AT_BN;
                     tma_load_2d(dst, &tm_kc, fb, it.h * kPrefillDh, yk, pol);
                     tma_load_2d(dst + BOX, &tm_kc, fb, it.h * kPrefillDh + 64, yk, pol);
@@ -365,8 +397,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     const int32_t p1 = page_at(a.page_row, 2 * j + 1, a.pages, a.num_pages, a.status);
                     tma_load_2d(dst + 2 * BOX, &tm_kr, fb, kPrefillDc, p0 * 64, pol);
                     tma_load_2d(dst + 2 * BOX + BOX / 2, &tm_kr, fb, kPrefillDc, p1 * 64, pol);
-                    tma_load_2d(dst + AT_K_BYTES, &tm_v, fb, it.h * kPrefillDh, yk, pol);
-                    tma_load_2d(dst + AT_K_BYTES + BOX, &tm_v, fb, it.h * kPrefillDh + 64, yk, pol);
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == AT_NST) {
@@ -376,28 +406,60 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 }
             }
             for (int s = 0; s < AT_NST; ++s)
-                if (issued & (1u << s)) drain_wait(bar(A_KVFULL + s), (last_par >> s) & 1u);
+                if (issued & (1u << s)) drain_wait(bar(A_KFULL + s), (last_par >> s) & 1u);
             if (qn > 0) drain_wait(bar(A_QFULL), (qn - 1) & 1u);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------- TMA (values)
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int32_t w = blockIdx.x; w < items && ok; w += gridDim.x) {
+                const Item it = item_of(w, m_tiles, a.H);
+                for (int32_t j = 0; j < it.ntiles; ++j) {
+                    ok = bounded_wait(bar(A_VEMPTY + stage), phase ^ 1u, abort_flag, a.status);
+                    if (!ok) break;
+                    const uint32_t fb = bar(A_VFULL + stage);
+                    const uint32_t dst = sbase + AT_OFF_V + stage * AT_V_BYTES;
+                    mbar_arrive_expect_tx(fb, AT_V_BYTES);
+                    const int32_t yk = j * AT_BN;
+                    tma_load_2d(dst, &tm_v, fb, it.h * kPrefillDh, yk, pol);
+                    tma_load_2d(dst + BOX, &tm_v, fb, it.h * kPrefillDh + 64, yk, pol);
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == AT_NST) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < AT_NST; ++s)
+                if (issued & (1u << s)) drain_wait(bar(A_VFULL + s), (last_par >> s) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0, pv_stage = 0, qn = 0, g = 0, items_done = 0;
+            uint32_t stage = 0, phase = 0, pv_stage = 0, pv_phase = 0, qn = 0, g = 0, items_done = 0;
             bool ok = true;
             const uint32_t tO = tmem + TM_O;
             auto issue_pv = [&](uint32_t gp, bool first) -> bool {
                 const uint32_t slot = gp & 1u;
                 if (!bounded_wait(bar(A_PFULL + slot), (gp >> 1) & 1u, abort_flag, a.status)) return false;
+                if (!bounded_wait(bar(A_VFULL + pv_stage), pv_phase, abort_flag, a.status)) return false;
                 tc_fence_after();
                 const uint32_t tP = tmem + TM_S0 + 128u * slot;
-                const uint32_t sv = sbase + AT_OFF_KV + pv_stage * AT_STAGE + AT_K_BYTES;
+                const uint32_t sv = sbase + AT_OFF_V + pv_stage * AT_V_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < AT_BN / 16; ++kk)
                     umma_ts(tO, tP + kk * 8, smem_desc(sv + kk * 2048, BOX, 1024, kSwizzle128B), AT_IDESC_PV,
                             (first && kk == 0) ? 0u : 1u);
                 umma_commit(bar(A_PVDONE + slot));
-                umma_commit(bar(A_KVEMPTY + pv_stage));
-                if (++pv_stage == AT_NST) pv_stage = 0;
+                umma_commit(bar(A_VEMPTY + pv_stage));
+                if (++pv_stage == AT_NST) {
+                    pv_stage = 0;
+                    pv_phase ^= 1u;
+                }
                 return true;
             };
             for (int32_t w = blockIdx.x; w < items && ok; w += gridDim.x) {
@@ -407,7 +469,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 ++qn;
                 for (int32_t j = 0; j < it.ntiles && ok; ++j, ++g) {
                     const uint32_t slot = g & 1u;
-                    ok = bounded_wait(bar(A_KVFULL + stage), phase, abort_flag, a.status);
+                    ok = bounded_wait(bar(A_KFULL + stage), phase, abort_flag, a.status);
                     if (!ok) break;
                     // the score buffer's previous tile (g - 2): its P was read by PV
                     if (g >= 2) {
@@ -416,7 +478,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t tS = tmem + TM_S0 + 128u * slot;
-                    const uint32_t sk = sbase + AT_OFF_KV + stage * AT_STAGE;
+                    const uint32_t sk = sbase + AT_OFF_K + stage * AT_K_BYTES;
 #pragma unroll
                     for (int c = 0; c < 3; ++c)
 #pragma unroll
@@ -425,6 +487,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                                     smem_desc(sk + c * BOX + kk * 32, 16, 1024, kSwizzle128B), AT_IDESC_QK,
                                     (c | kk) ? 1u : 0u);
                     umma_commit(bar(A_SFULL + slot));
+                    umma_commit(bar(A_KEMPTY + stage));   // the key stage is free once this QK completes
                     if (j == it.ntiles - 1) umma_commit(bar(A_QEMPTY));
                     if (++stage == AT_NST) {
                         stage = 0;
@@ -450,21 +513,46 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             umma_commit(bar(A_EXIT));
             drain_wait(bar(A_EXIT), 0);
         }
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_SOFTMAX_REGS));
         // ---------------------------------------------------- softmax / epilogue
+        // Two warpgroups take alternate key tiles (group g & 1 owns global
+        // tile g), so one tile's softmax overlaps the next tile's.  One
+        // thread owns one query row.  The running maximum is handed from the
+        // owner of tile g-1 to the owner of tile g through shared memory
+        // (A_MREADY); each group keeps the row sum of its own tiles relative
+        // to the latest maximum it has seen, and the owner of an item's last
+        // tile merges the other group's sum (A_LFULL / A_LFREE) and writes
+        // the epilogue.
+        const uint32_t wg = (uint32_t)((warp - 4) >> 2);
         const uint32_t q = (uint32_t)(warp & 3);
         const int32_t row = (int32_t)(q * 32 + lane);
         const uint32_t lane_off = (q * 32u) << 16;
         const uint32_t tO = tmem + TM_O + lane_off;
         const float sl2 = a.scale_log2;
-        uint32_t g = 0;
+        float* mrow = reinterpret_cast<float*>(smem + AT_OFF_M);     // [2 slots][128 rows]
+        float2* lm = reinterpret_cast<float2*>(smem + AT_OFF_LM);    // [2 items][128 rows]
+        uint32_t g = 0, k = 0;   // global tile and item counters of this CTA
         bool ok = true;
-        for (int32_t w = blockIdx.x; w < items && ok; w += gridDim.x) {
+        for (int32_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++k) {
             const Item it = item_of(w, m_tiles, a.H);
             const int32_t t = it.qt * AT_BM + row;    // this thread's query position
-            float m = -INFINITY, l = 0.f;
+            float m_seen = -INFINITY, l = 0.f;
             for (int32_t j = 0; j < it.ntiles && ok; ++j, ++g) {
                 const uint32_t slot = g & 1u;
+                const bool last = j == it.ntiles - 1;
+                if (slot != wg) {
+                    // not ours; after the item's last tile hand this group's sum over
+                    if (last) {
+                        ok = warp_wait(bar(A_LFREE + (k & 1u)), ((k >> 1) & 1u) ^ 1u, abort_flag, a.status);
+                        if (!ok) break;
+                        lm[(k & 1u) * 128 + row] = make_float2(l, m_seen);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(A_LFULL + (k & 1u)));
+                    }
+                    continue;
+                }
                 ok = warp_wait(bar(A_SFULL + slot), (g >> 1) & 1u, abort_flag, a.status);
                 if (!ok) break;
                 tc_fence_after();
@@ -495,16 +583,29 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < AT_BN; ++c) mx = fmaxf(mx, s[c]);
                 mx *= sl2;
-                float factor = 1.f;
+                // running maximum after tile g-1 (the other group's); lazy:
+                // it moves, and O is rescaled, only when it grows by > 2^8
+                float m_prev = -INFINITY;
+                if (g > 0) {
+                    ok = warp_wait(bar(A_MREADY + (slot ^ 1u)), ((g - 1) >> 1) & 1u, abort_flag, a.status);
+                    if (!ok) break;
+                    if (j > 0) m_prev = mrow[(slot ^ 1u) * 128 + row];
+                }
+                float m_cur = m_prev, factor = 1.f;
                 bool rescale = false;
-                if (mx > m + kRescale) {
-                    if (m != -INFINITY) {
-                        factor = fast_exp2(m - mx);
+                if (mx > m_prev + kRescale) {
+                    if (m_prev != -INFINITY) {
+                        factor = fast_exp2(m_prev - mx);
                         rescale = true;
                     }
-                    m = mx;
+                    m_cur = mx;
                 }
-                const float neg_m = (m == -INFINITY) ? 0.f : -m;
+                mrow[slot * 128 + row] = m_cur;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(A_MREADY + slot));
+                if (m_seen != -INFINITY && m_cur != m_seen) l *= fast_exp2(m_seen - m_cur);
+                m_seen = m_cur;
+                const float neg_m = (m_cur == -INFINITY) ? 0.f : -m_cur;
                 float ls0 = 0.f, ls1 = 0.f;
                 uint32_t pk[AT_BN / 2];
 #pragma unroll
@@ -515,7 +616,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                     ls1 += p1;
                     pk[c / 2] = pack_bf16x2(p0, p1);
                 }
-                l = l * factor + (ls0 + ls1);
+                l += ls0 + ls1;
                 // O rescale (after the previous tile's PV, before this tile's)
                 if (__any_sync(0xffffffffu, rescale) && j > 0) {
                     ok = warp_wait(bar(A_PVDONE + (slot ^ 1u)), ((g - 1) >> 1) & 1u, abort_flag, a.status);
@@ -548,35 +649,43 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(A_PFULL + slot));
-            }
-            if (!ok) break;
-            // epilogue: O / l after the item's last PV
-            ok = warp_wait(bar(A_PVDONE + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u, abort_flag, a.status);
-            if (!ok) break;
-            tc_fence_after();
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const bool store = t < a.T;
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)t * a.H + it.h) * kPrefillDh;
+                if (!last) continue;
+                // epilogue after the item's last PV: O / (both groups' sums)
+                ok = warp_wait(bar(A_PVDONE + slot), (g >> 1) & 1u, abort_flag, a.status);
+                if (!ok) break;
+                ok = warp_wait(bar(A_LFULL + (k & 1u)), (k >> 1) & 1u, abort_flag, a.status);
+                if (!ok) break;
+                const float2 other = lm[(k & 1u) * 128 + row];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(A_LFREE + (k & 1u)));
+                tc_fence_after();
+                // the other group's sum is relative to the maximum it last saw (<= m_seen)
+                const float l_tot = l + (other.y == -INFINITY ? 0.f : other.x * fast_exp2(other.y - m_seen));
+                const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                const bool store = t < a.T;
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)t * a.H + it.h) * kPrefillDh;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kPrefillDh; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tO + c0, r);
-                tmem_ld_wait32(r);
-                if (store) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+                for (int c0 = 0; c0 < kPrefillDh; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c0, r);
+                    tmem_ld_wait32(r);
+                    if (store) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        d4[k] = make_uint4(
-                            pack_bf16x2(__uint_as_float(r[8 * k]) * inv_l, __uint_as_float(r[8 * k + 1]) * inv_l),
-                            pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv_l, __uint_as_float(r[8 * k + 3]) * inv_l),
-                            pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv_l, __uint_as_float(r[8 * k + 5]) * inv_l),
-                            pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv_l, __uint_as_float(r[8 * k + 7]) * inv_l));
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            d4[k4] = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[8 * k4]) * inv_l, __uint_as_float(r[8 * k4 + 1]) * inv_l),
+                                pack_bf16x2(__uint_as_float(r[8 * k4 + 2]) * inv_l, __uint_as_float(r[8 * k4 + 3]) * inv_l),
+                                pack_bf16x2(__uint_as_float(r[8 * k4 + 4]) * inv_l, __uint_as_float(r[8 * k4 + 5]) * inv_l),
+                                pack_bf16x2(__uint_as_float(r[8 * k4 + 6]) * inv_l, __uint_as_float(r[8 * k4 + 7]) * inv_l));
+                    }
                 }
+                if (store && a.lse)
+                    a.lse[(int64_t)t * a.H + it.h] = l_tot > 0.f ? (m_seen + log2f(l_tot)) * kLn2f : -INFINITY;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(A_OFREE));
             }
-            if (store && a.lse) a.lse[(int64_t)t * a.H + it.h] = l > 0.f ? (m + log2f(l)) * kLn2f : -INFINITY;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(A_OFREE));
         }
     }
     tc_fence_before();
@@ -603,6 +712,12 @@ cudaError_t launch_prefill_attn(const PrefillAttnMaps& maps, const PrefillAttnAr
                                 cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
     if (e != cudaSuccess) return e;
+    // the register split must fit what the launch allocates, or the softmax
+    // warpgroups' setmaxnreg.inc could never be granted
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, prefill_attn_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * AT_THREADS < 32 * (4 * AT_PRODUCER_REGS + 8 * AT_SOFTMAX_REGS)) return cudaErrorInvalidConfiguration;
     const int32_t items = ((a.T + AT_BM - 1) / AT_BM) * a.H;
     const int32_t grid = items < sms ? items : sms;
     if (grid <= 0) return cudaSuccess;
