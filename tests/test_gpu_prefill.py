@@ -74,6 +74,17 @@ def test_prefill_paged_sixteen_heads():
     _compare(w, inp, out, lse)
 
 
+@pytest.mark.parametrize("H", [6, 12])
+def test_prefill_head_counts_that_change_the_work_order(H):
+    """Work items go head group by head group (8 heads when H allows, else
+    4 or 2; the projection needs an even H), and the two softmax warpgroups
+    take alternate key tiles, so these head counts change which group owns
+    which tile and which item finishes where."""
+    w = synth.prefill(T=300, H=H, seed=1250 + H)
+    out, lse, inp = _run_gpu(w)
+    _compare(w, inp, out, lse)
+
+
 def test_prefill_full_size_sampled_heads_and_rows():
     """T = 4096, H = 128 (the full-width decode's per-sequence shape); the
     oracle checks 5 heads (first, last, either side of the middle) at query
