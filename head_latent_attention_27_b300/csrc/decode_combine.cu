@@ -4,6 +4,7 @@
 // Units done by one piece were written by the attention kernel and are
 // skipped; units with no visible key get out = 0 and lse = -inf.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "decode_plan.cuh"
 
@@ -12,6 +13,21 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
+// Four consecutive partial values at element index idx of the partial rows
+// (fp16 rows from the tensor-core kernels, fp32 rows from the fp32 path).
+template <bool kF16>
+__device__ __forceinline__ float4 load_part4(const float* o_part, int64_t idx) {
+    if constexpr (kF16) {
+        const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(o_part) + idx);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+        return *reinterpret_cast<const float4*>(o_part + idx);
+    }
+}
+
+template <bool kF16Part>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     combine_kernel(int32_t Q, int32_t H, int32_t d_c, int32_t out_bf16, void* __restrict__ out,
                    float* __restrict__ lse, void* ws, WsLayout L) {
@@ -36,7 +52,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     // first two pieces' rows are issued together with the lse loads (one
     // memory round trip instead of two); the weights are applied after.
     const float* lp = v.lse_part + (int64_t)p0 * kRowsPerUnit + row;   // lse of piece k: lp[k * 128]
-    const float* ob = v.o_part + ((int64_t)p0 * kRowsPerUnit + row) * d_c;   // piece k: ob + k * 128 * d_c
+    const int64_t ob = ((int64_t)p0 * kRowsPerUnit + row) * d_c;   // element index; piece k: + k * 128 * d_c
     const int64_t pstride = (int64_t)kRowsPerUnit * d_c;
     constexpr int kChunks = 4;   // each lane owns up to 4 chunks of 4 columns (d_c <= 512, a multiple of 4)
     constexpr int kCached = 8;   // the lse of the first kCached pieces are loaded together
@@ -48,8 +64,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     for (int j = 0; j < kChunks; ++j) {
         const int32_t c0 = lane * 4 + 128 * j;
         const bool in = c0 < d_c;
-        x0[j] = in && n > 0 ? *reinterpret_cast<const float4*>(ob + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
-        x1[j] = in && n > 1 ? *reinterpret_cast<const float4*>(ob + pstride + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x0[j] = in && n > 0 ? load_part4<kF16Part>(v.o_part, ob + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x1[j] = in && n > 1 ? load_part4<kF16Part>(v.o_part, ob + pstride + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float m = -INFINITY;
 #pragma unroll
@@ -83,9 +99,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         for (int j = 0; j < kChunks; ++j) {
             const int32_t c0 = lane * 4 + 128 * j;
             const bool in = c0 < d_c;
-            y0[j] = in && w0 != 0.f ? *reinterpret_cast<const float4*>(ob + k0 * pstride + c0)
+            y0[j] = in && w0 != 0.f ? load_part4<kF16Part>(v.o_part, ob + k0 * pstride + c0)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            y1[j] = in && w1 != 0.f ? *reinterpret_cast<const float4*>(ob + k1 * pstride + c0)
+            y1[j] = in && w1 != 0.f ? load_part4<kF16Part>(v.o_part, ob + k1 * pstride + c0)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
@@ -127,8 +143,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 
 }  // namespace
 
-cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t out_dtype, void* out,
-                           float* lse, void* ws, const WsLayout& L, cudaStream_t stream) {
+cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t out_dtype, bool f16_partials,
+                           void* out, float* lse, void* ws, const WsLayout& L, cudaStream_t stream) {
     const int32_t U = B * units_per_seq(Q, H);
     if (U == 0) return cudaSuccess;
     const int32_t rows = min(kRowsPerUnit, Q * H);
@@ -142,7 +158,9 @@ cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, Q, H, d_c, (int32_t)(out_dtype == 0), out, lse, ws, L);
+    if (f16_partials)
+        return cudaLaunchKernelEx(&cfg, combine_kernel<true>, Q, H, d_c, (int32_t)(out_dtype == 0), out, lse, ws, L);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<false>, Q, H, d_c, (int32_t)(out_dtype == 0), out, lse, ws, L);
 }
 
 }  // namespace mla

@@ -96,7 +96,7 @@ struct WsView {
     int32_t* piece_worker;
     int32_t* worker_begin;
     float* lse_part;   // [max_pieces][128]
-    float* o_part;     // [max_pieces][128][d_c]
+    float* o_part;     // [max_pieces][128][d_c] fp32 (fp32 path) or fp16 in the same space (tensor-core paths)
 };
 
 __host__ __device__ inline WsView ws_view(void* ws, const WsLayout& L) {
@@ -136,7 +136,9 @@ __device__ inline int32_t checked_len(const int32_t* seq_lens, int32_t b, int32_
 cudaError_t launch_plan(const int32_t* seq_lens, int32_t B, int32_t Q, int32_t H, int32_t n_split,
                         int32_t num_workers, int32_t max_tokens, void* ws, const WsLayout& L,
                         cudaStream_t stream);
-cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t out_dtype, void* out,
-                           float* lse, void* ws, const WsLayout& L, cudaStream_t stream);
+// f16_partials: the partial rows were written in fp16 (the tensor-core
+// kernels) rather than fp32 (the fp32 path).
+cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t out_dtype, bool f16_partials,
+                           void* out, float* lse, void* ws, const WsLayout& L, cudaStream_t stream);
 
 }  // namespace mla

@@ -30,6 +30,7 @@
 // records MLA_ERR_TIMEOUT, waits (time-limited) for its own copies in
 // flight and exits.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "decode_sh.cuh"
@@ -501,14 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (r1 < rows) a.lse[grow1] = lse1;
                 }
             } else {
-                float* op = v.o_part + (int64_t)pc.slot * kRowsPerUnit * 512;
+                // partial rows of a split unit, normalised, in fp16
+                __half* op = reinterpret_cast<__half*>(v.o_part) + (int64_t)pc.slot * kRowsPerUnit * 512;
 #pragma unroll
                 for (int n = 0; n < kPvTiles; ++n) {
                     const int32_t d = dbase + 8 * n;
                     if (r0 < rows)
-                        *reinterpret_cast<float2*>(op + r0 * 512 + d) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                        *reinterpret_cast<__half2*>(op + r0 * 512 + d) = __floats2half2_rn(o[n][0] * inv0, o[n][1] * inv0);
                     if (r1 < rows)
-                        *reinterpret_cast<float2*>(op + r1 * 512 + d) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                        *reinterpret_cast<__half2*>(op + r1 * 512 + d) = __floats2half2_rn(o[n][2] * inv1, o[n][3] * inv1);
                 }
                 if (wq == 0 && c == 0) {
                     float* lp = v.lse_part + (int64_t)pc.slot * kRowsPerUnit;

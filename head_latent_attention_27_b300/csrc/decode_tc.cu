@@ -888,14 +888,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv_l, __uint_as_float(r[8 * q + 5]) * inv_l),
                                     pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv_l, __uint_as_float(r[8 * q + 7]) * inv_l));
                         } else {
-                            float4* dst = reinterpret_cast<float4*>(
-                                v.o_part + ((int64_t)slot_out * kRowsPerUnit + row) * 512 + col0 + c0);
+                            // partial row of a split unit, normalised, in fp16 (a convex
+                            // combination of cache rows: well inside fp16's range)
+                            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(v.o_part) +
+                                                                  ((int64_t)slot_out * kRowsPerUnit + row) * 512 +
+                                                                  col0 + c0);
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                dst[q] = make_float4(__uint_as_float(r[4 * q]) * inv_l,
-                                                     __uint_as_float(r[4 * q + 1]) * inv_l,
-                                                     __uint_as_float(r[4 * q + 2]) * inv_l,
-                                                     __uint_as_float(r[4 * q + 3]) * inv_l);
+                            for (int q = 0; q < 4; ++q)
+                                dst[q] = make_uint4(
+                                    pack_f16x2(__uint_as_float(r[8 * q + 0]) * inv_l, __uint_as_float(r[8 * q + 1]) * inv_l),
+                                    pack_f16x2(__uint_as_float(r[8 * q + 2]) * inv_l, __uint_as_float(r[8 * q + 3]) * inv_l),
+                                    pack_f16x2(__uint_as_float(r[8 * q + 4]) * inv_l, __uint_as_float(r[8 * q + 5]) * inv_l),
+                                    pack_f16x2(__uint_as_float(r[8 * q + 6]) * inv_l, __uint_as_float(r[8 * q + 7]) * inv_l));
                         }
                     }
                 }
