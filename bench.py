@@ -294,6 +294,7 @@ def run_cuda(args, w):
     import torch
 
     import head_latent_attention_27_b300 as mla
+    import synth
     from synth.device import empty_pool, to_torch, upload
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -445,118 +446,163 @@ def run_cuda(args, w):
                else torch.empty(tot, dtype=torch.uint8, device=device))
         views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
         return buf, views
-    # The staging buffer is written by ONE host thread: written by 16 threads
-    # its lines stayed dirty in the cores' private caches and the DMA reads
-    # that had to snoop them ran at 12-18 GB/s instead of 50-55 GB/s.
-    in_src = [d["q_nope"], d["q_rope"], new_c, new_k]
-    h_in, h_views = packed(in_src, None, True)
-    host_threads = torch.get_num_threads()
-    torch.set_num_threads(1)
-    for hv, t in zip(h_views, in_src):
-        hv.copy_(t.cpu())
-    torch.set_num_threads(host_threads)
-    n_sets = 2
-    d_in, d_qn, d_qr, d_c, d_k = [], [], [], [], []
-    h_outbuf, h_out, h_lse, d_outbuf, d_out, d_lse = [], [], [], [], [], []
-    for _ in range(n_sets):
-        buf, (a_, b_, c_, k_) = packed(in_src, dev, False)
-        d_in.append(buf); d_qn.append(a_); d_qr.append(b_); d_c.append(c_); d_k.append(k_)
-        buf, (o_, l_) = packed([out, lse], dev, False)
-        d_outbuf.append(buf); d_out.append(o_); d_lse.append(l_)
-        buf, (o_, l_) = packed([out, lse], None, True)
-        h_outbuf.append(buf); h_out.append(o_); h_lse.append(l_)
-    h2d = sum(t.numel() * t.element_size() for t in in_src)
-    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
     s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def compute(i):
+    def e2e_pipeline(in_src, out_src, compute):
+        """Times args.steps pipelined steps: per step one packed H2D of the
+        inputs (laid out like `in_src`, whose values they are), compute(i,
+        device input views, device output views) on buffer set i, one packed
+        D2H of the outputs (laid out like `out_src`).  Returns the timed
+        milliseconds (max over ranks), the host output views of every set,
+        the bytes per step each way and the link-only timings."""
+        # The staging buffer is written by ONE host thread: written by 16
+        # threads its lines stayed dirty in the cores' private caches and the
+        # DMA reads that had to snoop them ran at 12-18 GB/s instead of 50-55.
+        h_in, h_views = packed(in_src, None, True)
+        host_threads = torch.get_num_threads()
+        torch.set_num_threads(1)
+        for hv, t in zip(h_views, in_src):
+            hv.copy_(t.cpu())
+        torch.set_num_threads(host_threads)
+        n_sets = 2
+        d_in, d_in_v, d_outbuf, d_out_v, h_outbuf, h_out_v = [], [], [], [], [], []
+        for _ in range(n_sets):
+            buf, views = packed(in_src, dev, False)
+            d_in.append(buf); d_in_v.append(views)
+            buf, views = packed(out_src, dev, False)
+            d_outbuf.append(buf); d_out_v.append(views)
+            buf, views = packed(out_src, None, True)
+            h_outbuf.append(buf); h_out_v.append(views)
+        h2d = sum(t.numel() * t.element_size() for t in in_src)
+        d2h = sum(t.numel() * t.element_size() for t in out_src)
+        with torch.cuda.stream(s_comp):
+            for i in range(n_sets):      # eager warm-up of both buffer sets
+                d_in[i].copy_(h_in, non_blocking=True)
+                compute(i, d_in_v[i], d_out_v[i])
+        torch.cuda.synchronize(dev)
+        g_comp = []
+        for i in range(n_sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                compute(i, d_in_v[i], d_out_v[i])
+            g_comp.append(g)
+        torch.cuda.synchronize(dev)
+        ev_in = [torch.cuda.Event() for _ in range(n_sets)]
+        ev_comp = [torch.cuda.Event() for _ in range(n_sets)]
+        ev_out = [torch.cuda.Event() for _ in range(n_sets)]
+
+        def run_pipeline(n_steps, t0=None, t1=None):
+            if t0 is not None:
+                t0.record(s_in)
+            for step in range(n_steps):
+                i = step % n_sets
+                with torch.cuda.stream(s_in):
+                    if step >= n_sets:
+                        s_in.wait_event(ev_comp[i])          # set i's inputs consumed by step - 2
+                    d_in[i].copy_(h_in, non_blocking=True)
+                    ev_in[i].record(s_in)
+                with torch.cuda.stream(s_comp):
+                    s_comp.wait_event(ev_in[i])
+                    if step >= n_sets:
+                        s_comp.wait_event(ev_out[i])         # set i's outputs read back by step - 2
+                    g_comp[i].replay()
+                    ev_comp[i].record(s_comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_comp[i])
+                    h_outbuf[i].copy_(d_outbuf[i], non_blocking=True)
+                    ev_out[i].record(s_out)
+            if t1 is not None:
+                s_out.wait_stream(s_in)
+                s_out.wait_stream(s_comp)
+                t1.record(s_out)
+
+        run_pipeline(max(args.warmup, n_sets))
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        run_pipeline(args.steps, t0, t1)
+        torch.cuda.synchronize(dev)
+        tot = max_over_ranks(t0.elapsed_time(t1), dist, dev)
+
+        # the host link alone: the same copies with no compute, each
+        # direction alone and both together
+        def copies_ms(h2d_on: bool, d2h_on: bool) -> float:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record(s_in)
+            s_out.wait_stream(s_in)
+            for step in range(args.steps):
+                i = step % n_sets
+                if h2d_on:
+                    with torch.cuda.stream(s_in):
+                        d_in[i].copy_(h_in, non_blocking=True)
+                if d2h_on:
+                    with torch.cuda.stream(s_out):
+                        h_outbuf[i].copy_(d_outbuf[i], non_blocking=True)
+            s_in.wait_stream(s_out)
+            b.record(s_in)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / args.steps
+
+        copies_ms(True, True)   # warm
+        link = {"h2d": copies_ms(True, False), "d2h": copies_ms(False, True), "both": copies_ms(True, True)}
+        last = h_out_v[(args.steps - 1) % n_sets]
+        return tot, last, h2d, d2h, link
+
+    def compute(i, ins, outs):
         # plan beside the append (it reads only seq_lens), then attend + combine
+        qn, qr, c_new, k_new = ins
+        o_, l_ = outs
         cur = torch.cuda.current_stream(dev)
         s_side.wait_stream(cur)
         with torch.cuda.stream(s_side):
             mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws, n_split=n_split)
-        mla.mla_cache_append(cache, d_c[i], d_k[i], new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
+        mla.mla_cache_append(cache, c_new, k_new, new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
         cur.wait_stream(s_side)
-        mla.mla_decode_attend(cache, d["seq_lens"], d_qn[i], d_qr[i], d_out[i], ws, lse=d_lse[i], n_split=n_split,
-                              softmax_scale=scale)
-        mla.mla_decode_combine(cache, d_out[i], ws, lse=d_lse[i], n_split=n_split)
+        mla.mla_decode_attend(cache, d["seq_lens"], qn, qr, o_, ws, lse=l_, n_split=n_split, softmax_scale=scale)
+        mla.mla_decode_combine(cache, o_, ws, lse=l_, n_split=n_split)
 
-    with torch.cuda.stream(s_comp):
-        for i in range(n_sets):      # eager warm-up of both buffer sets
-            d_in[i].copy_(h_in, non_blocking=True)
-            compute(i)
-    torch.cuda.synchronize(dev)
-    g_comp = []
-    for i in range(n_sets):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            compute(i)
-        g_comp.append(g)
-    torch.cuda.synchronize(dev)
-    ev_in = [torch.cuda.Event() for _ in range(n_sets)]
-    ev_comp = [torch.cuda.Event() for _ in range(n_sets)]
-    ev_out = [torch.cuda.Event() for _ in range(n_sets)]
-
-    def run_pipeline(n_steps, t0=None, t1=None):
-        if t0 is not None:
-            t0.record(s_in)
-        for step in range(n_steps):
-            i = step % n_sets
-            with torch.cuda.stream(s_in):
-                if step >= n_sets:
-                    s_in.wait_event(ev_comp[i])          # set i's inputs consumed by step - 2
-                d_in[i].copy_(h_in, non_blocking=True)
-                ev_in[i].record(s_in)
-            with torch.cuda.stream(s_comp):
-                s_comp.wait_event(ev_in[i])
-                if step >= n_sets:
-                    s_comp.wait_event(ev_out[i])         # set i's outputs read back by step - 2
-                g_comp[i].replay()
-                ev_comp[i].record(s_comp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[i])
-                h_outbuf[i].copy_(d_outbuf[i], non_blocking=True)
-                ev_out[i].record(s_out)
-        if t1 is not None:
-            s_out.wait_stream(s_in)
-            s_out.wait_stream(s_comp)
-            t1.record(s_out)
-
-    run_pipeline(max(args.warmup, n_sets))
-    torch.cuda.synchronize(dev)
-    if dist is not None:
-        dist.barrier()
-    e2e_t0, e2e_t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    run_pipeline(args.steps, e2e_t0, e2e_t1)
-    torch.cuda.synchronize(dev)
-    e2e_tot = max_over_ranks(e2e_t0.elapsed_time(e2e_t1), dist, dev)
+    e2e_tot, (h_out_last, h_lse_last), h2d, d2h, link = e2e_pipeline(
+        [d["q_nope"], d["q_rope"], new_c, new_k], [out, lse], compute)
     # the last step's result came back and matches the device-resident run
-    if not (torch.equal(h_out[(args.steps - 1) % n_sets], out.cpu()) and
-            torch.equal(h_lse[(args.steps - 1) % n_sets], lse.cpu())):
+    if not (torch.equal(h_out_last, out.cpu()) and torch.equal(h_lse_last, lse.cpu())):
         raise RuntimeError("e2e result differs from the device-resident step")
 
-    # the host link alone: the same copies with no compute, each direction
-    # alone and both together, so that the e2e rate can be read against it
-    def copies_ms(h2d_on: bool, d2h_on: bool) -> float:
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        a.record(s_in)
-        s_out.wait_stream(s_in)
-        for step in range(args.steps):
-            i = step % n_sets
-            if h2d_on:
-                with torch.cuda.stream(s_in):
-                    d_in[i].copy_(h_in, non_blocking=True)
-            if d2h_on:
-                with torch.cuda.stream(s_out):
-                    h_outbuf[i].copy_(d_outbuf[i], non_blocking=True)
-        s_in.wait_stream(s_out)
-        b.record(s_in)
-        torch.cuda.synchronize(dev)
-        return a.elapsed_time(b) / args.steps
+    # ---- the same step with the layer's own inputs and outputs: the
+    #      per-head query q^C (d_h = 128) crosses the link instead of the
+    #      absorbed q_nope (d_c = 512), and the per-head output o = W^UV u
+    #      instead of the latent u; both absorption GEMMs run on the device
+    #      inside the timed region (synthetic seeded weights W^UK, W^UV)
+    bf = lambda shape, st, sc: to_torch(synth.normal(2024, st, int(np.prod(shape)), sc, 0, "bf16").reshape(shape),
+                                        "bf16", device=dev)
+    n_rows = w.B * w.Q
+    w_uk, w_uv = bf((w.H, w.d_h, w.d_c), 1, 1 / math.sqrt(w.d_h)), bf((w.H, w.d_h, w.d_c), 2, 1 / math.sqrt(w.d_c))
+    q_c = bf((n_rows, w.H, w.d_h), 3, 1.0)
+    o_layer = torch.empty((n_rows, w.H, w.d_h), dtype=torch.bfloat16, device=dev)
+    qn_s = [torch.empty_like(d["q_nope"]) for _ in range(2)]
+    u_s = [torch.empty_like(out) for _ in range(2)]
 
-    copies_ms(True, True)   # warm
-    link_h2d, link_d2h, link_both = copies_ms(True, False), copies_ms(False, True), copies_ms(True, True)
+    def compute_layer(i, ins, outs):
+        qc_, qr, c_new, k_new = ins
+        o_, l_ = outs
+        mla.mla_absorb_query(w_uk, qc_, qn_s[i].view(n_rows, w.H, w.d_c))
+        compute(i, (qn_s[i], qr, c_new, k_new), (u_s[i], l_))
+        mla.mla_absorb_output(w_uv, u_s[i].view(n_rows, w.H, w.d_c), o_)
+
+    lay_tot, (h_o_last, h_l_last), lay_h2d, lay_d2h, lay_link = e2e_pipeline(
+        [q_c, d["q_rope"], new_c, new_k], [o_layer, lse], compute_layer)
+    # device-resident run of the same layer step, for the bit-exact check
+    lse_chk = torch.empty_like(lse)
+    with torch.cuda.stream(s_comp):
+        compute_layer(0, (q_c, d["q_rope"], new_c, new_k), (o_layer, lse_chk))
+    torch.cuda.synchronize(dev)
+    if not (torch.equal(h_o_last, o_layer.cpu()) and torch.equal(h_l_last, lse_chk.cpu())):
+        raise RuntimeError("layer-io e2e result differs from the device-resident run")
+    status = mla.mla_decode_read_status(ws)
+    if status != mla.MLA_OK:
+        raise RuntimeError(f"kernel status {mla.mla_status_string(status)}")
 
     if rank == 0:
         peaks, peak_kind = load_peaks()
@@ -621,8 +667,13 @@ def run_cuda(args, w):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i (two buffer sets); "
                                  "one packed pinned copy per direction and step",
-                    "copies_only_ms_per_step": {"h2d": link_h2d, "d2h": link_d2h, "both": link_both},
-                    "link_gbs": {"h2d": h2d / link_h2d / 1e6, "d2h": d2h / link_d2h / 1e6}},
+                    "copies_only_ms_per_step": link,
+                    "link_gbs": {"h2d": h2d / link["h2d"] / 1e6, "d2h": d2h / link["d2h"] / 1e6}},
+            "e2e_layer_io": {"value": whole_job_rate(world, tokens_per_step, args.steps, lay_tot), "unit": UNIT,
+                             "h2d_bytes_per_step": lay_h2d, "d2h_bytes_per_step": lay_d2h,
+                             "work": "absorb_query (W^UK) + the step + absorb_output (W^UV) per step; inputs "
+                                     "q^C [B*Q, H, 128] + q_rope + new rows, outputs o [B*Q, H, 128] + lse",
+                             "copies_only_ms_per_step": lay_link},
             "phases_ms": {"append_and_plan": statistics.median(pre_ms), "attend": statistics.median(att_ms),
                           "combine": statistics.median(post_ms),
                           "note": "each phase replayed as a graph of its own (no overlap between phases)"},
