@@ -551,16 +551,24 @@ def run_cuda(args, w):
         last = h_out_v[(args.steps - 1) % n_sets]
         return tot, last, h2d, d2h, link
 
-    def compute(i, ins, outs):
-        # plan beside the append (it reads only seq_lens), then attend + combine
+    def compute(i, ins, outs, beside=None):
+        # plan beside the append (it reads only seq_lens), then attend +
+        # combine; beside(): more launches on a second side stream that the
+        # attention also waits for
         qn, qr, c_new, k_new = ins
         o_, l_ = outs
         cur = torch.cuda.current_stream(dev)
         s_side.wait_stream(cur)
         with torch.cuda.stream(s_side):
             mla.mla_decode_plan(cache, d["seq_lens"], w.Q, w.H, ws, n_split=n_split)
+        if beside is not None:
+            s_side2.wait_stream(cur)
+            with torch.cuda.stream(s_side2):
+                beside()
         mla.mla_cache_append(cache, c_new, k_new, new_seq, new_pos, eps=w.eps, rope_base=w.rope_base, flags=flags)
         cur.wait_stream(s_side)
+        if beside is not None:
+            cur.wait_stream(s_side2)
         mla.mla_decode_attend(cache, d["seq_lens"], qn, qr, o_, ws, lse=l_, n_split=n_split, softmax_scale=scale)
         mla.mla_decode_combine(cache, o_, ws, lse=l_, n_split=n_split)
 
@@ -584,11 +592,15 @@ def run_cuda(args, w):
     qn_s = [torch.empty_like(d["q_nope"]) for _ in range(2)]
     u_s = [torch.empty_like(out) for _ in range(2)]
 
+    s_side2 = torch.cuda.Stream(dev)
+
     def compute_layer(i, ins, outs):
+        # the query absorption depends only on q^C: it runs beside the plan
+        # and the append, and the attention waits for all three
         qc_, qr, c_new, k_new = ins
         o_, l_ = outs
-        mla.mla_absorb_query(w_uk, qc_, qn_s[i].view(n_rows, w.H, w.d_c))
-        compute(i, (qn_s[i], qr, c_new, k_new), (u_s[i], l_))
+        compute(i, (qn_s[i], qr, c_new, k_new), (u_s[i], l_),
+                beside=lambda: mla.mla_absorb_query(w_uk, qc_, qn_s[i].view(n_rows, w.H, w.d_c)))
         mla.mla_absorb_output(w_uv, u_s[i].view(n_rows, w.H, w.d_c), o_)
 
     lay_tot, (h_o_last, h_l_last), lay_h2d, lay_d2h, lay_link = e2e_pipeline(
@@ -671,7 +683,8 @@ def run_cuda(args, w):
                     "link_gbs": {"h2d": h2d / link["h2d"] / 1e6, "d2h": d2h / link["d2h"] / 1e6}},
             "e2e_layer_io": {"value": whole_job_rate(world, tokens_per_step, args.steps, lay_tot), "unit": UNIT,
                              "h2d_bytes_per_step": lay_h2d, "d2h_bytes_per_step": lay_d2h,
-                             "work": "absorb_query (W^UK) + the step + absorb_output (W^UV) per step; inputs "
+                             "work": "absorb_query (W^UK, beside the append and plan) + the step + absorb_output "
+                                     "(W^UV) per step; inputs "
                                      "q^C [B*Q, H, 128] + q_rope + new rows, outputs o [B*Q, H, 128] + lse",
                              "copies_only_ms_per_step": lay_link},
             "phases_ms": {"append_and_plan": statistics.median(pre_ms), "attend": statistics.median(att_ms),
