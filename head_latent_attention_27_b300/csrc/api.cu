@@ -314,7 +314,8 @@ mla_status_t do_combine(const mla_cache_t* c, DecodeShape s, void* out, float* l
     if (s.B == 0) return MLA_OK;
     // the low-precision cache decodes into bf16 output like the bf16 cache
     const int32_t out_dtype = c->dtype == MLA_FP32 ? MLA_FP32 : MLA_BF16;
-    return cuda_status(launch_combine(s.B, s.Q, s.H, c->d_c, out_dtype, c->dtype != MLA_FP32, out, lse, ws, L, stream));
+    return cuda_status(
+        launch_combine(s.B, s.Q, s.H, c->d_c, out_dtype, c->dtype != MLA_FP32, d->sms, out, lse, ws, L, stream));
 }
 
 mla_status_t run_decode(const mla_cache_t* c, const int32_t* seq_lens, DecodeShape s, const void* q_nope,

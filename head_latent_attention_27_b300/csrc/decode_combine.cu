@@ -14,20 +14,45 @@ namespace {
 constexpr int kWarpsPerBlock = 8;
 
 // Four consecutive partial values at element index idx of the partial rows
-// (fp16 rows from the tensor-core kernels, fp32 rows from the fp32 path).
+// (fp16 rows from the tensor-core kernels, fp32 rows from the fp32 path),
+// as loaded (Raw) and as floats.
 template <bool kF16>
-__device__ __forceinline__ float4 load_part4(const float* o_part, int64_t idx) {
+struct PartRaw {
+    using T = float4;
+};
+template <>
+struct PartRaw<true> {
+    using T = uint2;
+};
+
+template <bool kF16>
+__device__ __forceinline__ typename PartRaw<kF16>::T load_raw4(const float* o_part, int64_t idx) {
     if constexpr (kF16) {
-        const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(o_part) + idx);
-        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-        return make_float4(a.x, a.y, b.x, b.y);
+        return *reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(o_part) + idx);
     } else {
         return *reinterpret_cast<const float4*>(o_part + idx);
     }
 }
 
-template <bool kF16Part>
+template <bool kF16>
+__device__ __forceinline__ float4 raw_to_f4(typename PartRaw<kF16>::T u) {
+    if constexpr (kF16) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+        return u;
+    }
+}
+
+template <bool kF16>
+__device__ __forceinline__ float4 load_part4(const float* o_part, int64_t idx) {
+    return raw_to_f4<kF16>(load_raw4<kF16>(o_part, idx));
+}
+
+// kHeld: pieces whose rows are loaded in the first round trip (8 when the
+// grid is small enough that the extra registers cost no residency)
+template <bool kF16Part, int kHeld>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     combine_kernel(int32_t Q, int32_t H, int32_t d_c, int32_t out_bf16, void* __restrict__ out,
                    float* __restrict__ lse, void* ws, WsLayout L) {
@@ -49,8 +74,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int64_t grow = (int64_t)b * QH + (int64_t)rb * kRowsPerUnit + row;
 
     // Every piece of the unit wrote finite partial rows, so the loads of the
-    // first two pieces' rows are issued together with the lse loads (one
-    // memory round trip instead of two); the weights are applied after.
+    // first kHeld pieces' rows are issued together with the lse loads (one
+    // memory round trip for a unit of up to kHeld pieces: fp16 rows take 8
+    // registers per piece and lane); the weights are applied after.
     const float* lp = v.lse_part + (int64_t)p0 * kRowsPerUnit + row;   // lse of piece k: lp[k * 128]
     const int64_t ob = ((int64_t)p0 * kRowsPerUnit + row) * d_c;   // element index; piece k: + k * 128 * d_c
     const int64_t pstride = (int64_t)kRowsPerUnit * d_c;
@@ -59,13 +85,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     float lc[kCached];
 #pragma unroll
     for (int k = 0; k < kCached; ++k) lc[k] = k < n ? lp[(int64_t)k * kRowsPerUnit] : -INFINITY;
-    float4 x0[kChunks], x1[kChunks];
+    static_assert(kHeld == 2 || kHeld == kCached, "held pieces");
+    using Raw = typename PartRaw<kF16Part>::T;
+    Raw xr[kHeld][kChunks];
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) {
-        const int32_t c0 = lane * 4 + 128 * j;
-        const bool in = c0 < d_c;
-        x0[j] = in && n > 0 ? load_part4<kF16Part>(v.o_part, ob + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
-        x1[j] = in && n > 1 ? load_part4<kF16Part>(v.o_part, ob + pstride + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kHeld; ++k) {
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+            const int32_t c0 = lane * 4 + 128 * j;
+            xr[k][j] = (c0 < d_c && k < n) ? load_raw4<kF16Part>(v.o_part, ob + (int64_t)k * pstride + c0) : Raw{};
+        }
     }
     float m = -INFINITY;
 #pragma unroll
@@ -84,13 +113,27 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 #pragma unroll
     for (int k = 0; k < kCached; ++k)
         wc[k] = (k < n && total_lse != -INFINITY && lc[k] != -INFINITY) ? expf(lc[k] - total_lse) : 0.f;
+    // pieces past n hold zeros and weigh 0
     float4 acc[kChunks];
 #pragma unroll
     for (int j = 0; j < kChunks; ++j) {
-        acc[j].x = wc[0] * x0[j].x + wc[1] * x1[j].x;
-        acc[j].y = wc[0] * x0[j].y + wc[1] * x1[j].y;
-        acc[j].z = wc[0] * x0[j].z + wc[1] * x1[j].z;
-        acc[j].w = wc[0] * x0[j].w + wc[1] * x1[j].w;
+        const float4 x0 = raw_to_f4<kF16Part>(xr[0][j]), x1 = raw_to_f4<kF16Part>(xr[1][j]);
+        acc[j].x = wc[0] * x0.x + wc[1] * x1.x;
+        acc[j].y = wc[0] * x0.y + wc[1] * x1.y;
+        acc[j].z = wc[0] * x0.z + wc[1] * x1.z;
+        acc[j].w = wc[0] * x0.w + wc[1] * x1.w;
+    }
+#pragma unroll
+    for (int k = 2; k < kHeld; k += 2) {
+        if (k >= n) break;
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+            const float4 y0 = raw_to_f4<kF16Part>(xr[k][j]), y1 = raw_to_f4<kF16Part>(xr[k + 1][j]);
+            acc[j].x += wc[k] * y0.x + wc[k + 1] * y1.x;
+            acc[j].y += wc[k] * y0.y + wc[k + 1] * y1.y;
+            acc[j].z += wc[k] * y0.z + wc[k + 1] * y1.z;
+            acc[j].w += wc[k] * y0.w + wc[k + 1] * y1.w;
+        }
     }
     // acc += w0 o_k0 + w1 o_k1 for the remaining pieces, two at a time
     auto accumulate2 = [&](int32_t k0, float w0, int32_t k1, float w1) {
@@ -113,7 +156,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         }
     };
 #pragma unroll
-    for (int k = 2; k < kCached; k += 2) {   // compile-time k: the weights stay in registers
+    for (int k = kHeld; k < kCached; k += 2) {   // compile-time k: the weights stay in registers
         if (k >= n) break;
         accumulate2(k, wc[k], k + 1 < n ? k + 1 : k, k + 1 < n ? wc[k + 1] : 0.f);
     }
@@ -144,7 +187,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 }  // namespace
 
 cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t out_dtype, bool f16_partials,
-                           void* out, float* lse, void* ws, const WsLayout& L, cudaStream_t stream) {
+                           int32_t num_sms, void* out, float* lse, void* ws, const WsLayout& L,
+                           cudaStream_t stream) {
     const int32_t U = B * units_per_seq(Q, H);
     if (U == 0) return cudaSuccess;
     const int32_t rows = min(kRowsPerUnit, Q * H);
@@ -158,9 +202,15 @@ cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (f16_partials)
-        return cudaLaunchKernelEx(&cfg, combine_kernel<true>, Q, H, d_c, (int32_t)(out_dtype == 0), out, lse, ws, L);
-    return cudaLaunchKernelEx(&cfg, combine_kernel<false>, Q, H, d_c, (int32_t)(out_dtype == 0), out, lse, ws, L);
+    const int32_t obf = (int32_t)(out_dtype == 0);
+    if (!f16_partials) return cudaLaunchKernelEx(&cfg, combine_kernel<false, 2>, Q, H, d_c, obf, out, lse, ws, L);
+    // Holding 8 pieces per lane takes ~120 registers (2 blocks per SM): worth
+    // it when the whole grid fits in one such wave (units split over many
+    // workers, e.g. few sequences or few heads), not on large grids.
+    const int64_t blocks = (int64_t)cfg.gridDim.x * cfg.gridDim.y;
+    if (blocks <= 2 * (int64_t)num_sms)
+        return cudaLaunchKernelEx(&cfg, combine_kernel<true, 8>, Q, H, d_c, obf, out, lse, ws, L);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<true, 2>, Q, H, d_c, obf, out, lse, ws, L);
 }
 
 }  // namespace mla

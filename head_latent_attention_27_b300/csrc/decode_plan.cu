@@ -59,11 +59,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     WsView v = ws_view(ws, L);
     const int32_t RB = units_per_seq(Q, H);
     const int32_t U = B * RB;
-    __shared__ int32_t s_tiles[kSmemUnits], s_cost[kSmemUnits], s_pw[kSmemPieces];
+    __shared__ int32_t s_tiles[kSmemUnits], s_cost[kSmemUnits], s_pw[kSmemPieces], s_pb[kSmemUnits + 1];
+    // unit_piece_begin is written to the workspace for the other kernels and,
+    // when it fits, mirrored here for pass 3 (no global round trip)
     int32_t* unit_tiles = U <= kSmemUnits ? s_tiles : v.unit_tiles;
     int32_t* unit_cost = U <= kSmemUnits ? s_cost : v.unit_cost;
     const int32_t QH = Q * H;
     const int tid = threadIdx.x;
+    const bool pb_smem = U <= kSmemUnits;
     if (tid == 0) {
         v.hdr->status = 0;
         v.hdr->num_units = U;
@@ -99,7 +102,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         if (u < U) {
             unit_tiles[u] = (int32_t)tiles;
             unit_cost[u] = (int32_t)(carry_cost + ex_cost);
-            if (n_split > 0) v.unit_piece_begin[u] = (int32_t)(carry_np + ex_np);
+            if (n_split > 0) {
+                v.unit_piece_begin[u] = (int32_t)(carry_np + ex_np);
+                if (pb_smem) s_pb[u] = (int32_t)(carry_np + ex_np);
+            }
         }
         carry_cost += tot_cost;
         carry_np += tot_np;
@@ -123,7 +129,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             }
             int64_t tot;
             const int64_t ex = block_exclusive_scan(np, &tot);
-            if (u < U) v.unit_piece_begin[u] = (int32_t)(carry_np + ex);
+            if (u < U) {
+                v.unit_piece_begin[u] = (int32_t)(carry_np + ex);
+                if (pb_smem) s_pb[u] = (int32_t)(carry_np + ex);
+            }
             carry_np += tot;
         }
     }
@@ -131,6 +140,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     int32_t* piece_worker = NP <= kSmemPieces ? s_pw : v.piece_worker;
     if (tid == 0) {
         v.unit_piece_begin[U] = (int32_t)NP;
+        if (pb_smem) s_pb[U] = (int32_t)NP;
         v.hdr->num_pieces = (int32_t)NP;
     }
     __syncthreads();
@@ -139,8 +149,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     for (int32_t u = tid; u < U; u += kPlanThreads) {
         const int32_t tiles = unit_tiles[u];
         if (tiles == 0) continue;
-        const int32_t p0 = v.unit_piece_begin[u];
-        const int32_t np = v.unit_piece_begin[u + 1] - p0;
+        const int32_t p0 = pb_smem ? s_pb[u] : v.unit_piece_begin[u];
+        const int32_t np = (pb_smem ? s_pb[u + 1] : v.unit_piece_begin[u + 1]) - p0;
         const int64_t a = unit_cost[u];
         if (n_split > 0) {
             const int32_t chunk = (int32_t)ceil_div64(tiles, n_split);

@@ -137,8 +137,10 @@ cudaError_t launch_plan(const int32_t* seq_lens, int32_t B, int32_t Q, int32_t H
                         int32_t num_workers, int32_t max_tokens, void* ws, const WsLayout& L,
                         cudaStream_t stream);
 // f16_partials: the partial rows were written in fp16 (the tensor-core
-// kernels) rather than fp32 (the fp32 path).
+// kernels) rather than fp32 (the fp32 path); num_sms: the device's SM count
+// (sizes the per-lane register depth of the merge against the grid).
 cudaError_t launch_combine(int32_t B, int32_t Q, int32_t H, int32_t d_c, int32_t out_dtype, bool f16_partials,
-                           void* out, float* lse, void* ws, const WsLayout& L, cudaStream_t stream);
+                           int32_t num_sms, void* out, float* lse, void* ws, const WsLayout& L,
+                           cudaStream_t stream);
 
 }  // namespace mla
