@@ -239,8 +239,11 @@ MLA_API size_t mla_decode_workspace_size(int32_t B, int32_t Q, int32_t H, int32_
  * mla_decode_attend runs the attention kernel and writes final rows into
  * out/lse and partial rows into the workspace; mla_decode_combine merges the
  * partial rows.  All three take the same workspace and the same n_split
- * (0 = balanced); the cache dtype selects the kernel (tensor-core path for
- * bf16, CUDA-core path for fp32).
+ * (0 = balanced); the cache dtype and the unit size select the kernel:
+ * bf16 or low-precision (E4M3) rows with more than 16 query rows per unit
+ * (Q * H > 16) take the two-SM tcgen05 kernel, bf16 rows with Q * H <= 16
+ * the single-SM warp-MMA kernel, fp32 rows the CUDA-core kernel.  Plan,
+ * attend and combine must see the same cache, Q, H and n_split.
  */
 MLA_API mla_status_t mla_decode_plan(const mla_cache_t* cache, const int32_t* seq_lens, int32_t B,
                              int32_t Q, int32_t H, int32_t n_split,
